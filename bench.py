@@ -1,0 +1,384 @@
+"""Benchmark: fused linear cross-entropy forward + backward tokens/s on GB300.
+
+One step = flce_forward + flce_backward (grad_out = 1.0) over one batch of the
+headline workload, N=65536 tokens (batch 8 x 8192), D=4096, V=128256, bf16, 5%
+ignored rows, mean reduction -- the Llama-3-8B language-model head of "Cutting LLM
+Memory by 84%: A Deep Dive into Fused Kernels" ("The Logit Bottleneck") and of the
+Liger-Kernel PR #1291 BT sweep. Inputs are synthetic (seeded, see workloads).
+
+Prints ONE JSON line (rank 0). Launch with torchrun for several GPUs: each rank runs
+its own replica of the workload (weak scaling, no collective on the data path).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on bounded samples of the same workload
+(the reference arm); it runs on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s at N=65536,D=4096,V=128256 bf16; % of bf16 TC peak; peak MB"
+UNIT = "tokens/s"
+# Liger-Kernel PR #1291: CuTe-DSL FLCE fwd+bwd p50 = 194 ms at BT=65536, V=128256, H=4096, bf16, on B200.
+PAGES_TOKENS_PER_S = 65536 / 0.194
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kernel_launches_per_step(N, D, V, reduction):
+    """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
+    backward prep + 3 GEMMs per vocabulary band + the dX cast."""
+    kBN = 256
+    vc = max(kBN, ((1 << 30) // (2 * N)) // kBN * kBN)
+    half = (((V + 1) // 2) + kBN - 1) // kBN * kBN
+    vc = min(vc, half)
+    bands = -(-V // vc)
+    fwd = 1 + 1 + (0 if reduction == "none" else 1)
+    bwd = 1 + 3 * bands + 1
+    return fwd + bwd, bands, vc
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample_rate(wl, X, W, y, rows: int):
+    """fp64 oracle fwd+bwd on the first `rows` rows with the full vocabulary; returns (tokens/s, seconds)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward_backward(X[:rows], W, y[:rows], wl.ignore_index, wl.label_smoothing, wl.zloss_scale,
+                            wl.reduction)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    X, W, y = make_inputs(wl)
+    rows = args.oracle_rows
+    rates, times = [], []
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, X, W, y, rows)
+    for _ in range(args.steps):
+        r, dt = oracle_sample_rate(wl, X, W, y, rows)
+        rates.append(r)
+        times.append(dt)
+    value = statistics.median(rates)
+    sample = (f"fp64 oracle fwd+bwd of {rows} rows x full V={wl.V} (D={wl.D}) per step; "
+              f"tokens/s = rows / time; {args.steps} steps after {args.warmup} warm-up")
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * wl.N / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D), uniform targets, 5% ignored)",
+        "config": {"workload": wl.name, "N": wl.N, "D": wl.D, "V": wl.V, "reduction": wl.reduction,
+                   "ignore_frac": wl.ignore_frac},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, wl, world, rank, local):
+    import linear_cross_entropy_tcgen05_gb300 as flce
+    flce.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    N, D, V = wl.N, wl.D, wl.V
+    X, W, y = make_inputs(wl, seed=wl.seed + 1000 * rank)
+    Xd, Wd, yd = X.to(dev), W.to(dev), y.to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ws_f = flce.flce_workspace_size(N, D, V, False)
+    ws_b = flce.flce_workspace_size(N, D, V, True)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(D, V, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ws = torch.empty(max(ws_f, ws_b), dtype=torch.uint8, device=dev)
+    opts = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+
+    def fwd():
+        flce.flce_forward(Xd, Wd, yd, loss, lse, ws, *opts, stream=stream)
+
+    def bwd():
+        flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, stream=stream)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    st = flce.flce_check_device_error(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device error after warm-up: {flce.flce_status_string(st)}")
+    peak_alloc = torch.cuda.max_memory_allocated(dev)
+    extra_bytes = peak_alloc - base_alloc
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    st = flce.flce_check_device_error(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device error in the timed region: {flce.flce_status_string(st)}")
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = world * N / (ms_step / 1000.0)
+
+    # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
+    Xh, Wh, yh = X.pin_memory(), W.pin_memory(), y.pin_memory()
+    loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
+    dX_h = torch.empty(N, D, dtype=torch.bfloat16).pin_memory()
+    dW_h = torch.empty(D, V, dtype=torch.float32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 5))
+    h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 4
+    d2h = 4 + dX_h.numel() * 2 + dW_h.numel() * 4
+    for it in range(1 + e2e_steps):
+        if it == 1:
+            barrier(world)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        Xd.copy_(Xh, non_blocking=True)
+        Wd.copy_(Wh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        fwd()
+        bwd()
+        loss_h.copy_(loss, non_blocking=True)
+        dX_h.copy_(dX, non_blocking=True)
+        dW_h.copy_(dW, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_value = world * N / (e2e_ms / 1000.0)
+
+    peaks, peak_kind = measured_peaks()
+    flops_step = 8.0 * N * D * V
+    fwd_avg = statistics.mean(fwd_ms)
+    fwd_gemm_tf = 2.0 * N * D * V / (fwd_avg / 1000.0) / 1e12
+    step_tf = flops_step / (ms_step / 1000.0) / 1e12
+    bwd_tf = 6.0 * N * D * V / (statistics.mean(bwd_ms) / 1000.0) / 1e12
+    burst = float(peaks["bf16_tflops"])
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction)
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, dt = oracle_sample_rate(wl, X, W, y, args.oracle_rows)
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd of {args.oracle_rows} rows x full V ({dt:.1f} s); tokens/s = rows/time"}
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "forward_gemm_traffic.json")
+    if os.path.exists(tr_path):
+        tr = json.load(open(tr_path))
+        if tr.get("kernel_source_hash") == _kernel_hash():
+            traffic = tr.get("bytes_per_launch")
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGES_TOKENS_PER_S, "dtype": "bf16",
+        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D) in bf16, uniform targets, 5% ignore_index)",
+        "config": {"workload": wl.name, "N": N, "D": D, "V": V, "reduction": wl.reduction,
+                   "ignore_frac": wl.ignore_frac, "grad_out": 1.0,
+                   "l2": "inputs larger than L2 (X 0.54 GB, W 1.05 GB > 129 MB); no flush",
+                   "parallelism": f"replicas x{world}", "vocab_band": vc, "bands": bands},
+        "pct_bf16_peak": 100.0 * step_tf / burst,
+        "tflops": step_tf,
+        "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms),
+        "peak_mb": {"total": peak_alloc / 2**20, "extra": extra_bytes / 2**20,
+                    "workspace": max(ws_f, ws_b) / 2**20,
+                    "logits_bf16_would_be": N * V * 2 / 2**20},
+        "roofline": {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
+                     "peak": burst, "unit": "TFLOP/s", "frac": fwd_gemm_tf / burst, "traffic": traffic,
+                     "peak_kind": f"{peak_kind} burst cuBLAS bf16",
+                     "algorithmic": "2*N*D*V flops per launch (forward call = GEMM + finalize)"},
+        "roofline_step": {"bound": "tensor", "achieved": step_tf, "peak": sustained, "unit": "TFLOP/s",
+                          "frac": step_tf / sustained, "peak_kind": f"{peak_kind} sustained cuBLAS bf16",
+                          "algorithmic": "8*N*D*V flops per step"},
+        "roofline_backward": {"achieved": bwd_tf, "unit": "TFLOP/s", "frac": bwd_tf / sustained},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(out), flush=True)
+
+
+def _kernel_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("flce_gemm.cu", "sm103_ptx.cuh", "flce_internal.h"):
+        p = os.path.join(ROOT, "linear_cross_entropy_tcgen05_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS))
+    ap.add_argument("--oracle-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, world, rank)
+        else:
+            run_ours(args, wl, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+/*
+ * flce.h -- C ABI of the GB300 (sm_103a) fused linear cross-entropy library.
+ *
+ * Fused linear cross-entropy (FLCE) computes the cross-entropy loss of
+ * softmax(X @ W) for hidden states X [N,D] and a vocabulary projection W [D,V]
+ * without ever holding the N x V logits in memory, and its gradients dX and dW.
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "Cutting LLM Memory by 84%: A Deep Dive into Fused Kernels" (blog post):
+ *        "The Logit Bottleneck" (shapes), "Definition and Forward Pass" (loss =
+ *        lse - target logit, online softmax), "Backward Pass" ("Matrix
+ *        Multiplication", "Cross-Entropy", "Fused Linear Cross-Entropy"), "Setup
+ *        and Target Logit Pre-computation" (ignore_index, default -100), "Path to
+ *        Production" (no atomics on dX; a dW pass that writes each block once).
+ *   [P3] NVIDIA TransformerEngine pull request #995 (label-smoothing rule of the
+ *        backward kernel; entry points that release the Python GIL).
+ *   [P4] Liger-Kernel pull request #1291, "[CuteDSL] FLCE: 2-SM online-softmax fast
+ *        path (Blackwell)", "Summary": store-free forward that keeps only the
+ *        per-row LSE and target logit; a backward that recomputes the softmax per
+ *        vocabulary tile and contracts dW over the token dimension; feature list
+ *        (label_smoothing, z-loss "lse_square_scale", ignore_index, mean/sum,
+ *        forward-only reduction 'none', refusal of 'none' with a gradient).
+ *
+ * Definitions (eps = label_smoothing, s = zloss_scale, valid(i) <=> y_i != ignore_index):
+ *   z_ij   = sum_k X_ik W_kj
+ *   lse_i  = log sum_j exp(z_ij)
+ *   l_i    = (1-eps)(lse_i - z_{i,y_i}) + eps (lse_i - (1/V) sum_j z_ij) + s lse_i^2   (valid rows)
+ *   l_i    = 0                                                                         (ignored rows)
+ *   loss   = sum_i l_i  (SUM) | sum_i l_i / n_valid (MEAN, 0 if n_valid == 0) | l (NONE)
+ *   dZ_ij  = g [exp(z_ij - lse_i)(1 + 2 s lse_i) - (1-eps) delta_{j,y_i} - eps/V],
+ *            g = grad_out (SUM) or grad_out / n_valid (MEAN); dZ_i = 0 for ignored rows
+ *   dX     = dZ W^T,   dW = X^T dZ
+ * eps follows torch's convention: the target class keeps 1 - eps + eps/V of the
+ * probability mass, every other class eps/V. (TransformerEngine's label_smoothing
+ * alpha equals eps = alpha V / (V - 1).)
+ *
+ * Data layout (all row-major, contiguous, device memory):
+ *   X        bf16  [N, D]      row stride D elements
+ *   W        bf16  [D, V]      row stride V elements (note: not nn.Linear's [V, D])
+ *   targets  int32 [N]
+ *   lse      fp32  [N]
+ *   loss     fp32  [1] (MEAN, SUM) or [N] (NONE)
+ *   dX       bf16  [N, D]
+ *   dW       fp32  [D, V]
+ *
+ * Ownership and execution: the caller owns every buffer, including the
+ * workspace; the library never allocates or frees memory. All calls are
+ * asynchronous on `stream` and never synchronise, except
+ * flce_check_device_error. The library keeps no state between calls other than
+ * per-device launch attributes; separate workspaces make calls independent.
+ *
+ * Errors: host-side argument checks return a status synchronously and launch
+ * nothing. Conditions found on the device (a target outside [0, V) that is not
+ * the ignore index; a pipeline wait that exceeded its time limit) set an error
+ * word inside the workspace and poison the affected results with NaN; no kernel
+ * traps. flce_check_device_error reads that word.
+ *
+ * Requirements: a compute capability 10.3 device (GB300); D % 8 == 0 and
+ * V % 8 == 0 (16-byte row strides for the tensor-memory-access unit); X, W, dX,
+ * dW and the workspace 16-byte aligned; targets, lse and loss 4-byte aligned.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *`; NULL means the legacy default stream */
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,          /* null pointer, size < 1, eps outside [0,1), s < 0, bad enum */
+  FLCE_ERR_ALIGNMENT = 2,            /* D or V not a multiple of 8, or a misaligned pointer */
+  FLCE_ERR_UNSUPPORTED_DEVICE = 3,   /* the current device is not compute capability 10.3 */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 4,  /* ws_bytes < flce_workspace_size(...) */
+  FLCE_ERR_REDUCTION_NONE_GRAD = 5,  /* flce_backward with FLCE_REDUCTION_NONE (refused by design) */
+  FLCE_ERR_CUDA = 6,                 /* a CUDA runtime or driver call failed */
+  FLCE_ERR_BAD_TARGET = 7,           /* device: a target outside [0,V) that is not ignore_index */
+  FLCE_ERR_TIMEOUT = 8,              /* device: a pipeline wait exceeded its limit; results invalid */
+  FLCE_ERR_TOO_LARGE = 9             /* a size exceeds the library's index range */
+} flce_status;
+
+typedef enum {
+  FLCE_REDUCTION_MEAN = 0,
+  FLCE_REDUCTION_SUM = 1,
+  FLCE_REDUCTION_NONE = 2
+} flce_reduction;
+
+/* Bytes of workspace that flce_forward (for_backward == 0) or flce_backward
+ * (for_backward != 0) needs for this shape on the current device. Returns 0 for
+ * invalid sizes. The backward workspace holds a bf16 gradient band of N x Vc
+ * columns (Vc < V, a multiple of 256) and an fp32 [N, D] dX accumulator; no
+ * buffer has N x V elements. */
+size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward);
+
+/* Forward pass. [P1] "Definition and Forward Pass" and "Kernel Implementation"
+ * (online softmax over vocabulary tiles, target logit, lse - z_y); [P4] "Summary"
+ * (store-free: only the per-row LSE and target logit leave the GEMM epilogue).
+ *   X, W, targets : inputs as laid out above (device pointers).
+ *   ignore_index  : rows whose target equals it have loss 0 (default -100 in [P1]).
+ *   label_smoothing in [0,1), zloss_scale >= 0, red : see the definitions above.
+ *   loss          : out, fp32 [1] (MEAN/SUM) or [N] (NONE).
+ *   lse           : out, fp32 [N], log-sum-exp of every row (ignored rows included).
+ *   workspace     : device scratch of at least flce_workspace_size(N,D,V,0) bytes.
+ * Returns FLCE_OK or a host-side error; nothing is launched on error. */
+flce_status flce_forward(const void* X, const void* W, const int32_t* targets,
+                         int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                         float label_smoothing, float zloss_scale, flce_reduction red,
+                         float* loss, float* lse,
+                         void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Backward pass. [P1] "Backward Pass" and "Path to Production"; [P3] backward
+ * kernel (smoothing rule); [P4] "Summary" (recompute the softmax per vocabulary
+ * tile; dW contracts over the token dimension and each dW block is written once).
+ *   lse       : fp32 [N] from flce_forward with the same inputs.
+ *   grad_out  : device fp32 scalar, the upstream gradient of the reduced loss.
+ *   dX        : out, bf16 [N, D] (overwritten).
+ *   dW        : out, fp32 [D, V] (overwritten, each element written once).
+ *   workspace : device scratch of at least flce_workspace_size(N,D,V,1) bytes.
+ * The options must equal the forward call's. FLCE_REDUCTION_NONE is refused
+ * (FLCE_ERR_REDUCTION_NONE_GRAD), as in [P4]: a per-row upstream gradient is not
+ * supported by the fused reduction. */
+flce_status flce_backward(const void* X, const void* W, const int32_t* targets, const float* lse,
+                          int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                          float label_smoothing, float zloss_scale, flce_reduction red,
+                          const float* grad_out, void* dX, float* dW,
+                          void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * most recent call that used `workspace`. Returns FLCE_OK, FLCE_ERR_BAD_TARGET,
+ * FLCE_ERR_TIMEOUT, or FLCE_ERR_CUDA if the copy itself failed. */
+flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream);
+
+/* A static, human-readable name for a status. */
+const char* flce_status_string(flce_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int flce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

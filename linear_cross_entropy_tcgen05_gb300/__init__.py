@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) fused linear cross-entropy.
+
+A thin Python binding over the C ABI in ``include/flce.h`` (``libflce.so``, built
+in-tree by ``build.py``). The functions ``flce_forward``, ``flce_backward``,
+``flce_workspace_size``, ``flce_check_device_error`` and ``flce_status_string``
+marshal torch tensors into pointers and sizes and call the library; every step of
+the computation runs in the library's CUDA kernels. There is no CPU fallback: if
+the library is missing, ``load_library`` raises.
+
+``linear_cross_entropy`` wraps the two calls in a ``torch.autograd.Function``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "FLCEError", "load_library", "library_path", "flce_workspace_size", "flce_forward", "flce_backward",
+    "flce_check_device_error", "flce_status_string", "flce_version", "linear_cross_entropy",
+    "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
+STATUS = {
+    0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_ALIGNMENT", 3: "FLCE_ERR_UNSUPPORTED_DEVICE",
+    4: "FLCE_ERR_WORKSPACE_TOO_SMALL", 5: "FLCE_ERR_REDUCTION_NONE_GRAD", 6: "FLCE_ERR_CUDA",
+    7: "FLCE_ERR_BAD_TARGET", 8: "FLCE_ERR_TIMEOUT", 9: "FLCE_ERR_TOO_LARGE",
+}
+EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
+                    "flce_status_string", "flce_version")
+
+
+class FLCEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{where}: {flce_status_string(status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libflce.so")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libflce.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with `python -m linear_cross_entropy_tcgen05_gb300.build`")
+    lib = ctypes.CDLL(p)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.flce_workspace_size.argtypes = [i64, i64, i64, ctypes.c_int]
+    lib.flce_workspace_size.restype = sz
+    lib.flce_forward.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, vp, vp, vp, sz, vp]
+    lib.flce_forward.restype = ctypes.c_int
+    lib.flce_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, vp, vp, vp, vp,
+                                  sz, vp]
+    lib.flce_backward.restype = ctypes.c_int
+    lib.flce_check_device_error.argtypes = [vp, vp]
+    lib.flce_check_device_error.restype = ctypes.c_int
+    lib.flce_status_string.argtypes = [ctypes.c_int]
+    lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_version.argtypes = []
+    lib.flce_version.restype = ctypes.c_int
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def flce_status_string(status: int) -> str:
+    return load_library().flce_status_string(int(status)).decode()
+
+
+def flce_version() -> int:
+    return int(load_library().flce_version())
+
+
+def flce_workspace_size(N: int, D: int, V: int, for_backward: bool) -> int:
+    return int(load_library().flce_workspace_size(N, D, V, 1 if for_backward else 0))
+
+
+def logits_bytes(N: int, V: int, elem_bytes: int) -> int:
+    """Bytes of an N x V logits buffer (what the fused path never allocates)."""
+    return int(N) * int(V) * int(elem_bytes)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr() if isinstance(t, torch.Tensor) else int(t)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise FLCEError(status, where)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size() if isinstance(t, torch.Tensor) else 0
+
+
+def flce_forward(X, W, targets, loss, lse, workspace, ignore_index: int = -100, label_smoothing: float = 0.0,
+                 zloss_scale: float = 0.0, reduction: str = "mean", stream=None, N=None, D=None, V=None,
+                 ws_bytes=None, raise_on_error: bool = True) -> int:
+    """Call flce_forward. Tensors are device tensors laid out as in flce.h; returns the status."""
+    N = X.shape[0] if N is None else N
+    D = X.shape[1] if D is None else D
+    V = W.shape[1] if V is None else V
+    st = load_library().flce_forward(
+        _ptr(X), _ptr(W), _ptr(targets), N, D, V, int(ignore_index), float(label_smoothing), float(zloss_scale),
+        REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction), _ptr(loss), _ptr(lse),
+        _ptr(workspace), _nbytes(workspace) if ws_bytes is None else int(ws_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_forward")
+    return st
+
+
+def flce_backward(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_index: int = -100,
+                  label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean", stream=None,
+                  N=None, D=None, V=None, ws_bytes=None, raise_on_error: bool = True) -> int:
+    """Call flce_backward (grad_out is a device fp32 scalar tensor); returns the status."""
+    N = X.shape[0] if N is None else N
+    D = X.shape[1] if D is None else D
+    V = W.shape[1] if V is None else V
+    st = load_library().flce_backward(
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), N, D, V, int(ignore_index), float(label_smoothing),
+        float(zloss_scale), REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction),
+        _ptr(grad_out), _ptr(dX), _ptr(dW), _ptr(workspace),
+        _nbytes(workspace) if ws_bytes is None else int(ws_bytes), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_backward")
+    return st
+
+
+def flce_check_device_error(workspace, stream=None) -> int:
+    """Synchronise and read/clear the device error word; returns the status code."""
+    return int(load_library().flce_check_device_error(_ptr(workspace), _stream(stream)))
+
+
+def _workspace(N, D, V, device, for_backward, cache=None):
+    need = flce_workspace_size(N, D, V, for_backward)
+    if cache is not None and cache.numel() >= need:
+        return cache
+    return torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+
+
+def _validate(X, W, targets):
+    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("X and W must be bfloat16")
+    if targets.dtype != torch.int32:
+        raise TypeError("targets must be int32")
+    if X.dim() != 2 or W.dim() != 2 or targets.dim() != 1 or X.shape[1] != W.shape[0] or X.shape[0] != targets.shape[0]:
+        raise ValueError("expected X [N,D], W [D,V], targets [N]")
+    if not (X.is_cuda and W.is_cuda and targets.is_cuda):
+        raise ValueError("X, W and targets must be CUDA tensors")
+    if not (X.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
+        raise ValueError("X, W and targets must be contiguous")
+
+
+class LinearCrossEntropyFunction(torch.autograd.Function):
+    """loss = CE(softmax(X @ W), targets) with fused tensor-core kernels (no N x V logits)."""
+
+    @staticmethod
+    def forward(ctx, X, W, targets, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean"):
+        _validate(X, W, targets)
+        N, D = X.shape
+        V = W.shape[1]
+        ws = _workspace(N, D, V, X.device, False)
+        loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
+        lse = torch.empty(N, dtype=torch.float32, device=X.device)
+        flce_forward(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction)
+        ctx.save_for_backward(X, W, targets, lse)
+        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction)
+        return loss if reduction == "none" else loss[0]
+
+    @staticmethod
+    def backward(ctx, grad_loss):
+        X, W, targets, lse = ctx.saved_tensors
+        ignore_index, label_smoothing, zloss_scale, reduction = ctx.opts
+        if reduction == "none":
+            raise RuntimeError("reduction='none' has no fused backward (FLCE_ERR_REDUCTION_NONE_GRAD)")
+        N, D = X.shape
+        V = W.shape[1]
+        ws = _workspace(N, D, V, X.device, True)
+        g = grad_loss.detach().to(device=X.device, dtype=torch.float32).reshape(1).contiguous()
+        dX = torch.empty_like(X)
+        dW = torch.empty(D, V, dtype=torch.float32, device=X.device)
+        flce_backward(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction)
+        return dX, dW.to(W.dtype), None, None, None, None, None
+
+
+def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,
+                         zloss_scale: float = 0.0, reduction: str = "mean"):
+    """Fused linear cross-entropy of X [N,D] (bf16), W [D,V] (bf16), int32 targets [N].
+
+    The gradient of W is accumulated in fp32 by the kernels and returned in W's dtype
+    through autograd; call ``flce_backward`` directly to keep the fp32 dW.
+    """
+    return LinearCrossEntropyFunction.apply(X, W, targets, ignore_index, label_smoothing, zloss_scale, reduction)

@@ -1,0 +1,385 @@
+// flce_api.cu -- the C ABI (include/flce.h): argument checks, workspace layout,
+// tensor-map encoding and the launch sequence of the forward and backward passes.
+//
+// Forward  ("Cutting LLM Memory by 84%", "Definition and Forward Pass"; Liger-Kernel
+//           PR #1291 "Summary", store-free forward):
+//   1. tensor-core GEMM over (row tile, vocabulary range) units with the online-softmax
+//      epilogue -> partial (max, sum-exp, sum-z) per row and range, target logit;
+//   2. finalize: combine the partials -> lse, row losses, deterministic reduction.
+// Backward ("Backward Pass" and "Path to Production" of the same post; PR #1291: dW
+//           contracts over the tokens and is written once):
+//   1. prep: number of valid rows, g, per-row coefficients;
+//   2. for every band of Vc vocabulary columns:
+//        gradient GEMM : recompute the logits, G = dZ in bf16 into the band;
+//        dW GEMM       : dW[:, band] = X^T G   (K = N, each block written once);
+//        dX GEMM       : dX_acc (+)= G W[:, band]^T (fp32, TMA element-wise add);
+//   3. cast dX_acc to bf16.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/flce.h"
+#include "flce_internal.h"
+
+using namespace flce;
+
+namespace {
+
+constexpr size_t kHeaderBytes = 256;
+constexpr int64_t kGradBandBudget = int64_t(1) << 30;  // bytes of bf16 gradient band
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct FwdLayout {
+  size_t part_m, part_d, part_s, tgt, block_sum, block_cnt, total;
+  int S_alloc, blocks;
+};
+
+FwdLayout fwd_layout(int64_t N, int64_t V) {
+  FwdLayout L{};
+  const int64_t v_tiles = cdiv(V, kBN);
+  L.S_alloc = int(v_tiles < kMaxSplits ? v_tiles : kMaxSplits);
+  L.blocks = int(cdiv(N, kFinalizeThreads));
+  size_t o = kHeaderBytes;
+  const size_t part = align256(size_t(L.S_alloc) * size_t(N) * sizeof(float));
+  L.part_m = o; o += part;
+  L.part_d = o; o += part;
+  L.part_s = o; o += part;
+  L.tgt = o; o += align256(size_t(N) * sizeof(float));
+  L.block_sum = o; o += align256(size_t(L.blocks) * sizeof(double));
+  L.block_cnt = o; o += align256(size_t(L.blocks) * sizeof(int));
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  size_t coef, band, dx_acc, total;
+  int64_t Vc;
+};
+
+// Width of the gradient band: as many 256-column tiles as fit in the byte budget,
+// and never more than half the vocabulary (rounded up to a tile), so that no buffer
+// holds N x V values once V exceeds one tile.
+int64_t band_width(int64_t N, int64_t V) {
+  int64_t vc = (kGradBandBudget / (2 * N)) / kBN * kBN;
+  if (vc < kBN) vc = kBN;
+  const int64_t half = cdiv(cdiv(V, 2), kBN) * kBN;
+  if (vc > half) vc = half;
+  return vc;
+}
+
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
+  BwdLayout L{};
+  L.Vc = band_width(N, V);
+  size_t o = kHeaderBytes;
+  L.coef = o; o += align256(size_t(N) * 16);
+  L.band = o; o += align256(size_t(N) * size_t(L.Vc) * 2);
+  L.dx_acc = o; o += align256(size_t(N) * size_t(D) * sizeof(float));
+  L.total = o;
+  return L;
+}
+
+bool sizes_ok(int64_t N, int64_t D, int64_t V) { return N >= 1 && D >= 1 && V >= 1; }
+
+bool sizes_in_range(int64_t N, int64_t D, int64_t V) {
+  const int64_t lim = int64_t(1) << 30;
+  return N < lim && D < lim && V < lim;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// --- device and driver entry points ---------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct DevInfo {
+  bool known;
+  bool ok;
+  int sms;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+flce_status current_device(int* sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return FLCE_ERR_UNSUPPORTED_DEVICE;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (dev >= 64) return FLCE_ERR_UNSUPPORTED_DEVICE;
+  if (!g_dev[dev].known) {
+    int major = 0, minor = 0, n = 0;
+    bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+              cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    g_dev[dev].known = true;
+    g_dev[dev].ok = ok && major == 10 && minor == 3;
+    g_dev[dev].sms = n;
+  }
+  if (!g_dev[dev].ok) return FLCE_ERR_UNSUPPORTED_DEVICE;
+  *sms = g_dev[dev].sms;
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+// 2-D row-major tensor [outer][inner] with row pitch `pitch_elems`, 128-byte swizzled boxes.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch_elems * uint64_t(elem_bytes)};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+flce_status check_common(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
+                         float eps, float s, int red, const void* ws) {
+  if (!X || !W || !targets || !ws) return FLCE_ERR_INVALID_ARG;
+  if (!sizes_ok(N, D, V)) return FLCE_ERR_INVALID_ARG;
+  if (!(eps >= 0.f && eps < 1.f)) return FLCE_ERR_INVALID_ARG;
+  if (!(s >= 0.f) || std::isinf(s)) return FLCE_ERR_INVALID_ARG;
+  if (red < 0 || red > 2) return FLCE_ERR_INVALID_ARG;
+  if (!sizes_in_range(N, D, V)) return FLCE_ERR_TOO_LARGE;
+  if (D % 8 != 0 || V % 8 != 0) return FLCE_ERR_ALIGNMENT;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(ws, 16) || !aligned(targets, 4)) return FLCE_ERR_ALIGNMENT;
+  return FLCE_OK;
+}
+
+// Forward grid: gN row tiles x S vocabulary ranges = one CTA per SM.
+void pick_forward_grid(int sms, int64_t n_tiles, int64_t v_tiles, int S_alloc, int* gN_out, int* S_out) {
+  int gN = 1;
+  const int cands[4] = {8, 4, 2, 1};
+  for (int c : cands)
+    if (sms % c == 0 && sms / c <= kMaxSplits) {
+      gN = c;
+      break;
+    }
+  if (gN > n_tiles) gN = int(n_tiles);
+  int64_t S = sms / gN;
+  if (S > v_tiles) S = v_tiles;
+  if (S > S_alloc) S = S_alloc;
+  if (S < 1) S = 1;
+  *gN_out = gN;
+  *S_out = int(S);
+}
+
+#define FLCE_CUDA_CHECK(expr)                 \
+  do {                                        \
+    if ((expr) != cudaSuccess) {              \
+      cudaGetLastError();                     \
+      return FLCE_ERR_CUDA;                   \
+    }                                         \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int flce_version(void) { return 100; }
+
+const char* flce_status_string(flce_status st) {
+  switch (st) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARG: return "FLCE_ERR_INVALID_ARG: null pointer, bad size, option or enum";
+    case FLCE_ERR_ALIGNMENT: return "FLCE_ERR_ALIGNMENT: D and V must be multiples of 8 and pointers aligned";
+    case FLCE_ERR_UNSUPPORTED_DEVICE: return "FLCE_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+    case FLCE_ERR_WORKSPACE_TOO_SMALL: return "FLCE_ERR_WORKSPACE_TOO_SMALL";
+    case FLCE_ERR_REDUCTION_NONE_GRAD: return "FLCE_ERR_REDUCTION_NONE_GRAD: reduction 'none' has no fused backward";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA: a CUDA runtime or driver call failed";
+    case FLCE_ERR_BAD_TARGET: return "FLCE_ERR_BAD_TARGET: a target outside [0, V) that is not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT: a device pipeline wait exceeded its limit";
+    case FLCE_ERR_TOO_LARGE: return "FLCE_ERR_TOO_LARGE: a size exceeds 2^30";
+  }
+  return "unknown flce_status";
+}
+
+size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward) {
+  if (!sizes_ok(N, D, V) || !sizes_in_range(N, D, V)) return 0;
+  return for_backward ? bwd_layout(N, D, V).total : fwd_layout(N, V).total;
+}
+
+flce_status flce_forward(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
+                         int32_t ignore_index, float label_smoothing, float zloss_scale, flce_reduction red,
+                         float* loss, float* lse, void* workspace, size_t ws_bytes, struct CUstream_st* stream_) {
+  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
+  if (st != FLCE_OK) return st;
+  if (!loss || !lse) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(loss, 4) || !aligned(lse, 4)) return FLCE_ERR_ALIGNMENT;
+  const FwdLayout L = fwd_layout(N, V);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != FLCE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+
+  const int64_t n_tiles = cdiv(N, kBM), v_tiles = cdiv(V, kBN);
+  int gN = 1, S = 1;
+  pick_forward_grid(sms, n_tiles, v_tiles, L.S_alloc, &gN, &S);
+
+  CUtensorMap tmX, tmW;
+  if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) ||
+      !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, 64))
+    return FLCE_ERR_CUDA;
+
+  FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  FwdParams p{};
+  p.targets = targets;
+  p.N = int(N);
+  p.V = int(V);
+  p.n_tiles = int(n_tiles);
+  p.v_tiles = int(v_tiles);
+  p.gN = gN;
+  p.S = S;
+  p.num_kb = int(cdiv(D, kBK));
+  p.want_sum_z = label_smoothing != 0.f;
+  p.part_m = reinterpret_cast<float*>(ws + L.part_m);
+  p.part_d = reinterpret_cast<float*>(ws + L.part_d);
+  p.part_s = reinterpret_cast<float*>(ws + L.part_s);
+  p.tgt = reinterpret_cast<float*>(ws + L.tgt);
+  p.err = err;
+  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, stream));
+
+  FinalizeParams f{};
+  f.part_m = p.part_m;
+  f.part_d = p.part_d;
+  f.part_s = p.part_s;
+  f.tgt = p.tgt;
+  f.targets = targets;
+  f.N = int(N);
+  f.V = int(V);
+  f.S = S;
+  f.ignore_index = ignore_index;
+  f.eps = label_smoothing;
+  f.zscale = zloss_scale;
+  f.reduction = int(red);
+  f.lse = lse;
+  f.loss = loss;
+  f.block_sum = reinterpret_cast<double*>(ws + L.block_sum);
+  f.block_cnt = reinterpret_cast<int*>(ws + L.block_cnt);
+  f.err = err;
+  FLCE_CUDA_CHECK(launch_finalize(f, L.blocks, stream));
+  return FLCE_OK;
+}
+
+flce_status flce_backward(const void* X, const void* W, const int32_t* targets, const float* lse, int64_t N,
+                          int64_t D, int64_t V, int32_t ignore_index, float label_smoothing, float zloss_scale,
+                          flce_reduction red, const float* grad_out, void* dX, float* dW, void* workspace,
+                          size_t ws_bytes, struct CUstream_st* stream_) {
+  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
+  if (st != FLCE_OK) return st;
+  if (!lse || !grad_out || !dX || !dW) return FLCE_ERR_INVALID_ARG;
+  if (red == FLCE_REDUCTION_NONE) return FLCE_ERR_REDUCTION_NONE_GRAD;
+  if (!aligned(lse, 4) || !aligned(grad_out, 4) || !aligned(dX, 16) || !aligned(dW, 16)) return FLCE_ERR_ALIGNMENT;
+  const BwdLayout L = bwd_layout(N, D, V);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  st = current_device(&sms);
+  if (st != FLCE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  float* cval = reinterpret_cast<float*>(ws + 16);
+  float4* coef = reinterpret_cast<float4*>(ws + L.coef);
+  void* band = ws + L.band;
+  float* dx_acc = reinterpret_cast<float*>(ws + L.dx_acc);
+  const int64_t Vc = L.Vc;
+
+  CUtensorMap tmXk, tmXmn, tmWmn, tmWk, tmG, tmGmn, tmDW, tmDX;
+  const bool enc =
+      encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) &&
+      encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, 64) &&
+      encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, 64) &&
+      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, kBN) &&
+      encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, kBM) &&
+      encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, 64) &&
+      encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(V), uint64_t(D), uint64_t(V), 32, kBM) &&
+      encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_acc, uint64_t(D), uint64_t(N), uint64_t(D), 32, kBM);
+  if (!enc) return FLCE_ERR_CUDA;
+
+  FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  PrepParams pp{};
+  pp.targets = targets;
+  pp.lse = lse;
+  pp.grad_out = grad_out;
+  pp.N = int(N);
+  pp.V = int(V);
+  pp.ignore_index = ignore_index;
+  pp.eps = label_smoothing;
+  pp.zscale = zloss_scale;
+  pp.reduction = int(red);
+  pp.coef = coef;
+  pp.cval = cval;
+  pp.err = err;
+  FLCE_CUDA_CHECK(launch_prep(pp, stream));
+
+  const int64_t n_tiles = cdiv(N, kBM);
+  const int64_t d_tiles_m = cdiv(D, kBM);  // dW rows
+  const int64_t d_tiles_n = cdiv(D, kBN);  // dX columns
+  for (int64_t v0 = 0, band_i = 0; v0 < V; v0 += Vc, ++band_i) {
+    const int64_t vc = (V - v0 < Vc) ? V - v0 : Vc;
+    const int64_t vt = cdiv(vc, kBN);
+
+    WalkParams wg{};
+    wg.total_tiles = int(n_tiles * vt);
+    wg.tiles_minor = int(vt);
+    wg.num_kb = int(cdiv(D, kBK));
+    wg.b_row_off = int(v0);
+    GradEpiParams ge{coef, cval, int(N), int(V), int(v0), err};
+    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge,
+                                     int(wg.total_tiles < sms ? wg.total_tiles : sms), stream));
+
+    WalkParams ww{};
+    ww.total_tiles = int(vt * d_tiles_m);
+    ww.tiles_minor = int(d_tiles_m);
+    ww.num_kb = int(cdiv(N, kBK));
+    StoreEpiParams sw{0, int(v0), err};
+    FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw,
+                                   int(ww.total_tiles < sms ? ww.total_tiles : sms), stream));
+
+    WalkParams wx{};
+    wx.total_tiles = int(n_tiles * d_tiles_n);
+    wx.tiles_minor = int(d_tiles_n);
+    wx.num_kb = int(cdiv(vc, kBK));
+    wx.b_k0 = int(v0);
+    StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
+    FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx,
+                                   int(wx.total_tiles < sms ? wx.total_tiles : sms), stream));
+  }
+  FLCE_CUDA_CHECK(launch_cast_bf16(dx_acc, dX, size_t(N) * size_t(D), sms, stream));
+  return FLCE_OK;
+}
+
+flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream_) {
+  if (!workspace) return FLCE_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int word = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return FLCE_ERR_CUDA;
+  }
+  if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
+  if (word & FLCE_DEVERR_BAD_TARGET) return FLCE_ERR_BAD_TARGET;
+  return FLCE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared entry
+point, sizes its workspace, and refuses bad arguments before launching anything.
+
+No test here launches a kernel: the argument checks run before the device check.
+"""
+import json
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+import torch
+
+import linear_cross_entropy_tcgen05_gb300 as flce
+from linear_cross_entropy_tcgen05_gb300 import build as flce_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(flce.library_path()):
+        flce_build.build()
+    return flce.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(flce_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    fns = declared_functions()
+    for name in ("flce_forward", "flce_backward", "flce_workspace_size", "flce_check_device_error",
+                 "flce_status_string", "flce_version"):
+        assert name in fns
+    assert set(fns) == set(flce.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    nm = shutil.which("nm")
+    if nm:
+        out = subprocess.run([nm, "-D", "--defined-only", flce.library_path()], capture_output=True, text=True).stdout
+        exported = set(re.findall(r"\bT\s+(flce_\w+)", out))
+        assert set(declared_functions()) <= exported
+
+
+def test_version_and_status_strings(lib):
+    assert flce.flce_version() == 100
+    for code, name in flce.STATUS.items():
+        assert flce.flce_status_string(code).startswith(name)
+    assert "unknown" in flce.flce_status_string(99)
+
+
+def test_workspace_sizes(lib):
+    # forward: header + 3 partial arrays [S,N] + target logits + block sums; S = min(64, V/256 tiles)
+    ws = flce.flce_workspace_size(256, 128, 1024, False)
+    assert ws >= 3 * 4 * 256 * 4 + 256 * 4
+    assert flce.flce_workspace_size(0, 128, 1024, False) == 0
+    assert flce.flce_workspace_size(16, -1, 1024, True) == 0
+    # backward at the headline shape: a bf16 band of Vc < V columns plus the fp32 dX accumulator
+    N, D, V = 65536, 4096, 128256
+    wb = flce.flce_workspace_size(N, D, V, True)
+    logits_bf16 = flce.logits_bytes(N, V, 2)
+    assert wb < logits_bf16 / 4, "the backward workspace must be far below an N x V bf16 buffer"
+    assert wb >= N * D * 4  # holds the fp32 dX accumulator
+    # every band is narrower than the vocabulary once V exceeds one 256-column tile
+    for (n, d, v) in [(256, 128, 1024), (4096, 2048, 32000), (8192, 4096, 128256), (16384, 2304, 256000)]:
+        band = flce.flce_workspace_size(n, d, v, True) - n * d * 4 - n * 16 - 256
+        assert band < n * v * 2
+
+
+def test_logit_bottleneck_arithmetic():
+    """The page's sizes: 65,536 x 128,256 logits are ~8.4 B values, 16.8 GB bf16, 33.6 GB fp32."""
+    g = json.load(open(os.path.join(GOLDEN, "logit_bottleneck.json")))
+    n = g["N"] * g["V"]
+    assert round(n / 1e9, 1) == g["elements_billions"]
+    assert round(flce.logits_bytes(g["N"], g["V"], 2) / 1e9, 1) == g["bf16_GB"]
+    assert round(flce.logits_bytes(g["N"], g["V"], 4) / 1e9, 1) == g["fp32_GB"]
+
+
+class _Fake:
+    """A stand-in address with a chosen alignment; never dereferenced (checks fail first)."""
+
+    def __init__(self, addr):
+        self.addr = addr
+
+
+def _fwd(lib, X=0x10000, W=0x20000, y=0x30000, N=256, D=128, V=1024, eps=0.0, s=0.0, red=0, loss=0x40000,
+         lse=0x50000, ws=0x60000, wsb=None):
+    wsb = flce.flce_workspace_size(256, 128, 1024, False) if wsb is None else wsb
+    return lib.flce_forward(X, W, y, N, D, V, -100, eps, s, red, loss, lse, ws, wsb, None)
+
+
+def _bwd(lib, red=0, D=128, V=1024, grad=0x70000, wsb=None, X=0x10000):
+    wsb = flce.flce_workspace_size(256, D, V, True) if wsb is None else wsb
+    return lib.flce_backward(X, 0x20000, 0x30000, 0x50000, 256, D, V, -100, 0.0, 0.0, red, grad, 0x80000,
+                             0x90000, 0x60000, wsb, None)
+
+
+def test_forward_argument_checks(lib):
+    assert _fwd(lib, X=None) == 1
+    assert _fwd(lib, N=0) == 1
+    assert _fwd(lib, eps=1.0) == 1
+    assert _fwd(lib, eps=-0.1) == 1
+    assert _fwd(lib, eps=float("nan")) == 1
+    assert _fwd(lib, s=-1.0) == 1
+    assert _fwd(lib, s=float("inf")) == 1
+    assert _fwd(lib, red=3) == 1
+    assert _fwd(lib, loss=None) == 1
+    assert _fwd(lib, D=130) == 2      # D % 8
+    assert _fwd(lib, V=1001) == 2     # V % 8
+    assert _fwd(lib, X=0x10008) == 2  # 16-byte alignment
+    assert _fwd(lib, y=0x30002) == 2
+    assert _fwd(lib, N=1 << 31) == 9
+    assert _fwd(lib, wsb=16) == 4
+
+
+def test_backward_argument_checks(lib):
+    assert _bwd(lib, red=2) == 5      # reduction 'none' with a gradient is refused
+    assert _bwd(lib, grad=None) == 1
+    assert _bwd(lib, V=1004) == 2
+    assert _bwd(lib, X=0x10004) == 2
+    assert _bwd(lib, wsb=1024) == 4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the refusal on a machine without a GB300")
+def test_refuses_without_a_supported_device(lib):
+    assert _fwd(lib) == 3
+    assert _bwd(lib) == 3
+
+
+def test_python_wrapper_validates_dtypes():
+    X = torch.zeros(4, 8, dtype=torch.float32)
+    W = torch.zeros(8, 16, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(TypeError):
+        flce.linear_cross_entropy(X, W, y)
+    with pytest.raises(ValueError):
+        flce.linear_cross_entropy(X.bfloat16(), W, y)  # CPU tensors are refused, never computed on the host

@@ -141,6 +141,25 @@ const char* flce_status_string(flce_status status);
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int flce_version(void);
 
+/* Forward pass without a workspace, for callers that cannot allocate device memory
+ * (code inside an allocator or memory-pool callback, runtimes that give a fixed
+ * device arena and forbid further allocation). The source pages have no
+ * counterpart: this is a library convenience. Arguments, outputs and results are
+ * those of flce_forward; the scratch is a 64 MiB device array inside the library,
+ * taken on every GPU where this entry point is used until the process exits.
+ *  - The first call on a device (with that device current) looks up the array's
+ *    device address; make that first call before any stream capture.
+ *  - All calls share the array: calls that overlap on the GPU race; serialise them.
+ *    Each call clears the parts that must start at zero.
+ *  - Shapes needing more than 64 MiB of forward scratch (flce_workspace_size(N, D,
+ *    V, 0)) return FLCE_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ *  - It never calls cudaMalloc, cudaFree or any allocating routine. Device-detected
+ *    bad targets still poison the loss with NaN; the error word is internal. */
+flce_status flce_forward_noalloc(const void* X, const void* W, const int32_t* targets,
+                                 int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                                 float label_smoothing, float zloss_scale, flce_reduction red,
+                                 float* loss, float* lse, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

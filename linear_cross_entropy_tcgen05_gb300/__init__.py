@@ -32,7 +32,7 @@ STATUS = {
     7: "FLCE_ERR_BAD_TARGET", 8: "FLCE_ERR_TIMEOUT", 9: "FLCE_ERR_TOO_LARGE",
 }
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
-                    "flce_status_string", "flce_version")
+                    "flce_status_string", "flce_version", "flce_forward_noalloc")
 
 
 class FLCEError(RuntimeError):

@@ -213,12 +213,13 @@ def run_ours(args, wl, world, rank, local):
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     g = torch.ones(1, dtype=torch.float32, device=dev)
-    dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
-    dW = torch.empty(D, V, dtype=torch.float32, device=dev)
+    with_bwd = args.only != "fwd"
+    dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev) if with_bwd else None
+    dW = torch.empty(D, V, dtype=torch.float32, device=dev) if with_bwd else None
     torch.cuda.synchronize(dev)
     base_alloc = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    ws = torch.empty(max(ws_f, ws_b), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(ws_f, ws_b) if with_bwd else ws_f, dtype=torch.uint8, device=dev)
     opts = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
 
     def fwd():
@@ -226,6 +227,20 @@ def run_ours(args, wl, world, rank, local):
 
     def bwd():
         flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, stream=stream)
+
+    if args.only is not None:
+        # profiling driver: warm-up + steps of one phase, nothing else on the device
+        if args.only == "bwd":
+            fwd()
+        step = fwd if args.only == "fwd" else bwd
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize(dev)
+        st = flce.flce_check_device_error(ws, stream)
+        print(json.dumps({"only": args.only, "workload": wl.name, "status": flce.flce_status_string(st)}))
+        if st != 0:
+            raise SystemExit(1)
+        return
 
     for _ in range(args.warmup):
         fwd()
@@ -265,6 +280,16 @@ def run_ours(args, wl, world, rank, local):
     value = world * N / (ms_step / 1000.0)
 
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
+    e2e_value, e2e_ms, h2d, d2h = run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd)
+    return finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc,
+                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk)
+
+
+def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
+    if args.no_e2e:
+        return None, None, 0, 0
+    N, D = X.shape
+    V = W.shape[1]
     Xh, Wh, yh = X.pin_memory(), W.pin_memory(), y.pin_memory()
     loss_h = torch.empty(1, dtype=torch.float32).pin_memory()
     dX_h = torch.empty(N, D, dtype=torch.bfloat16).pin_memory()
@@ -291,7 +316,11 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     e2e_value = world * N / (e2e_ms / 1000.0)
+    return e2e_value, e2e_ms, h2d, d2h
 
+
+def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
+           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -364,10 +393,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS))
-    ap.add_argument("--oracle-rows", type=int, default=32)
+    ap.add_argument("--oracle-rows", type=int, default=512)
+    ap.add_argument("--shape", default=None, help="N,D,V override of the workload's shape (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--only", choices=["fwd", "bwd"], default=None,
+                    help="profiling driver: run only this phase (warm-up + steps), print a status line")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
+    if args.shape:
+        import dataclasses
+        n, d, v = (int(x) for x in args.shape.split(","))
+        wl = dataclasses.replace(wl, name=f"{wl.name}@{n}x{d}x{v}", N=n, D=d, V=v)
     world, rank, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libflce.so")
 
-SOURCES = ["flce_gemm.cu", "flce_api.cu", "flce_noalloc.cu"]
+SOURCES = ["flce_gemm.cu", "flce_small.cu", "flce_api.cu", "flce_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -161,17 +161,17 @@ flce_status check_common(const void* X, const void* W, const int32_t* targets, i
   return FLCE_OK;
 }
 
-// Forward grid: gN row tiles x S vocabulary ranges = one CTA per SM.
-void pick_forward_grid(int sms, int64_t n_tiles, int64_t v_tiles, int S_alloc, int* gN_out, int* S_out) {
+// Forward grid: gN row tiles x S vocabulary ranges = the resident CTA pairs.
+void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc, int* gN_out, int* S_out) {
   int gN = 1;
   const int cands[4] = {8, 4, 2, 1};
   for (int c : cands)
-    if (sms % c == 0 && sms / c <= kMaxSplits) {
+    if (units % c == 0 && units / c <= kMaxSplits) {
       gN = c;
       break;
     }
   if (gN > n_tiles) gN = int(n_tiles);
-  int64_t S = sms / gN;
+  int64_t S = units / gN;
   if (S > v_tiles) S = v_tiles;
   if (S > S_alloc) S = S_alloc;
   if (S < 1) S = 1;
@@ -230,9 +230,11 @@ flce_status flce_forward(const void* X, const void* W, const int32_t* targets, i
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* err = reinterpret_cast<int*>(ws);
 
-  const int64_t n_tiles = cdiv(N, kBM), v_tiles = cdiv(V, kBN);
+  const int64_t n_tiles = cdiv(N, gemm_tile_rows()), v_tiles = cdiv(V, kBN);
+  const int units = forward_max_units();
+  if (units <= 0) return FLCE_ERR_CUDA;
   int gN = 1, S = 1;
-  pick_forward_grid(sms, n_tiles, v_tiles, L.S_alloc, &gN, &S);
+  pick_forward_grid(units, n_tiles, v_tiles, L.S_alloc, &gN, &S);
 
   CUtensorMap tmX, tmW;
   if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) ||
@@ -307,7 +309,8 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
       encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) &&
       encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, 64) &&
       encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, 64) &&
-      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, kBN) &&
+      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64,
+                uint32_t(gemm_b_rows_per_cta())) &&
       encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, kBM) &&
       encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, 64) &&
       encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(V), uint64_t(D), uint64_t(V), 32, kBM) &&
@@ -330,9 +333,9 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
   pp.err = err;
   FLCE_CUDA_CHECK(launch_prep(pp, stream));
 
-  const int64_t n_tiles = cdiv(N, kBM);
-  const int64_t d_tiles_m = cdiv(D, kBM);  // dW rows
-  const int64_t d_tiles_n = cdiv(D, kBN);  // dX columns
+  const int64_t n_tiles = cdiv(N, gemm_tile_rows());
+  const int64_t d_tiles_m = cdiv(D, gemm_tile_rows());  // dW rows
+  const int64_t d_tiles_n = cdiv(D, kBN);               // dX columns
   for (int64_t v0 = 0, band_i = 0; v0 < V; v0 += Vc, ++band_i) {
     const int64_t vc = (V - v0 < Vc) ? V - v0 : Vc;
     const int64_t vt = cdiv(vc, kBN);
@@ -343,16 +346,14 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
     wg.num_kb = int(cdiv(D, kBK));
     wg.b_row_off = int(v0);
     GradEpiParams ge{coef, cval, int(N), int(V), int(v0), err};
-    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge,
-                                     int(wg.total_tiles < sms ? wg.total_tiles : sms), stream));
+    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, stream));
 
     WalkParams ww{};
     ww.total_tiles = int(vt * d_tiles_m);
     ww.tiles_minor = int(d_tiles_m);
     ww.num_kb = int(cdiv(N, kBK));
     StoreEpiParams sw{0, int(v0), err};
-    FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw,
-                                   int(ww.total_tiles < sms ? ww.total_tiles : sms), stream));
+    FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
 
     WalkParams wx{};
     wx.total_tiles = int(n_tiles * d_tiles_n);
@@ -360,8 +361,7 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
     wx.num_kb = int(cdiv(vc, kBK));
     wx.b_k0 = int(v0);
     StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
-    FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx,
-                                   int(wx.total_tiles < sms ? wx.total_tiles : sms), stream));
+    FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx, stream));
   }
   FLCE_CUDA_CHECK(launch_cast_bf16(dx_acc, dX, size_t(N) * size_t(D), sms, stream));
   return FLCE_OK;

@@ -1,36 +1,40 @@
 // flce_gemm.cu -- the tensor-core kernels of fused linear cross-entropy on sm_103a.
 //
-// All four GEMMs share one warp-specialised, persistent skeleton:
-//   warp 0      : TMA producer. One elected lane streams A and B K-blocks (64 bf16
-//                 deep, 128-byte swizzled) into a 4-stage shared-memory ring.
-//   warp 1      : MMA issuer. Allocates 512 TMEM columns (two 128x256 fp32
-//                 accumulators), issues tcgen05.mma (M=128, N=256, K=16) per stage
-//                 and commits each stage back to the producer and each finished
-//                 accumulator to the epilogue.
-//   warps 2..5  : epilogue. 128 threads, thread r owns TMEM lane r = output row r,
-//                 so every per-row reduction is thread-local. While they drain one
-//                 accumulator the MMA warp fills the other.
+// All four GEMMs share one warp-specialised, persistent skeleton, run by a pair of
+// CTAs on two SMs (a cluster of 2, tcgen05 cta_group::2) that together own a 256 x 256
+// output tile; each CTA holds 128 rows of it:
+//   warp 0      : TMA producer. One lane streams this CTA's 128 rows of A and its half
+//                 (128 columns) of B, 64-deep K blocks, 128-byte swizzled, into a
+//                 multi-stage ring; the completions land on the leader CTA's barrier.
+//   warp 1      : TMEM owner (both CTAs allocate 512 columns together: two 128x256
+//                 fp32 accumulators per CTA). In the leader CTA one lane issues
+//                 tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads both CTAs'
+//                 shared memory, and multicasts each stage's completion to both
+//                 producers and each finished accumulator to both epilogues.
+//   warps 2..5  : epilogue. Thread r owns TMEM lane r = output row r of its CTA, so every
+//                 per-row reduction is thread-local; the epilogue of one tile overlaps
+//                 the MMAs of the next.
+// A single-CTA variant (CG = 1, M = 128) is kept for comparison.
 //
 // The epilogues:
-//   forward   : online softmax over the tile's vocabulary columns (running max m,
-//               sum of exp(z - m), sum of z) and capture of the target logit; the
-//               logits never leave the chip. ("Cutting LLM Memory by 84%: A Deep
-//               Dive into Fused Kernels", "Definition and Forward Pass" and
-//               "Kernel Implementation"; Liger-Kernel PR #1291 "Summary": a
-//               store-free forward that keeps only the per-row LSE and target logit.)
+//   forward   : online softmax over the tile's vocabulary columns (running max m, sum
+//               of exp(z - m), sum of z) and capture of the target logit; the logits
+//               never leave the chip. ("Cutting LLM Memory by 84%: A Deep Dive into
+//               Fused Kernels", "Definition and Forward Pass" and "Kernel
+//               Implementation"; Liger-Kernel PR #1291 "Summary": a store-free forward
+//               that keeps only the per-row LSE and target logit.)
 //   gradient  : recomputed logits -> G = g[p(1+2s lse) - (1-eps) onehot - eps/V] in
 //               registers, rounded to bf16 and stored by TMA into the gradient band.
 //               ("Cross-Entropy" and "Fused Linear Cross-Entropy" of the same post;
 //               the smoothing rule of TransformerEngine PR #995's backward kernel.)
 //   dW / dX   : fp32 accumulator -> shared memory -> TMA store (dW, each block written
-//               once) or TMA element-wise add (dX accumulation across vocabulary
-//               bands, no atomics on the same element within a launch).
+//               once) or TMA element-wise add (dX accumulation across vocabulary bands,
+//               each element touched by one tile per launch, so no races).
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "flce_internal.h"
 #include "sm103_ptx.cuh"
-#include "vec_split.h"
 
 namespace flce {
 
@@ -38,9 +42,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { TILE_FIRST = 1, TILE_LAST = 2 };
 
+// Per CTA-group constants.
+template <int CG>
+struct Geo {
+  static constexpr int kRowsPerCta = kBM;             // A rows / TMEM lanes per CTA
+  static constexpr int kTileRows = kBM * CG;          // output rows per tile
+  static constexpr int kBRows = kBN / CG;             // B rows (K-major) or columns (MN-major) per CTA
+  static constexpr int kBBytesCta = kBRows * kBK * 2;
+  static constexpr int kStageBytesCta = kABytes + kBBytesCta;
+  static constexpr uint32_t kTxBytes = uint32_t(CG * kStageBytesCta);  // per stage, on the leader's barrier
+  static constexpr int kTemptyCount = CG == 1 ? kEpiThreads : CG * (kEpiThreads / 32);
+};
+
+template <int CG, int STAGES, int STAGING>
+constexpr size_t smem_bytes() {
+  return size_t(STAGES) * Geo<CG>::kStageBytesCta + size_t(STAGING) * kStagingBytes + kBarrierBytes + 1024;
+}
+
 struct Tile {
-  int a_row;   // A operand: first M row (K-major) or first M column (MN-major)
-  int b_row;   // B operand: first N row (K-major) or first N column (MN-major)
+  int a_row;   // this CTA's first A row (K-major) or column (MN-major): tile base + rank*128
+  int b_row;   // the tile's first B row/column (the CTA adds rank*kBRows when loading)
   int a_k0;    // K coordinate of the first K block in A
   int b_k0;    // ... and in B
   int num_kb;  // number of 64-wide K blocks
@@ -48,25 +69,47 @@ struct Tile {
   int flags;
 };
 
+struct Pair {
+  int cid;        // cluster (CTA pair) index
+  int nclusters;  // clusters in the grid
+  int rank;       // 0 = leader, 1 = peer (always 0 for CG = 1)
+};
+
+template <int CG>
+__device__ __forceinline__ Pair pair_id() {
+  Pair p;
+  p.cid = int(blockIdx.x) / CG;
+  p.nclusters = int(gridDim.x) / CG;
+  p.rank = CG == 1 ? 0 : int(cluster_ctarank());
+  return p;
+}
+
 // ---------------------------------------------------------------------------------
-// Tile schedules (every role of a CTA walks the same sequence)
+// Tile schedules (every role of both CTAs of a pair walks the same sequence)
 // ---------------------------------------------------------------------------------
 
-// Forward: the grid is gN row tiles x S vocabulary ranges. CTA c keeps row-tile
-// offset c % gN and walks groups of gN row tiles; in group g it covers vocabulary
-// range (c / gN + g) mod S, so the extra tile of the longer ranges rotates among
-// CTAs. Running statistics stay in registers across a range and are written once per
-// (row, range).
+// Forward: the clusters form gN row tiles x S vocabulary ranges. Cluster c keeps
+// row-tile offset c % gN and walks groups of gN row tiles; in group g it covers
+// vocabulary range (c / gN + g) mod S, so the extra tile of the longer ranges rotates
+// among clusters. Running statistics stay in registers across a range and are written
+// once per (row, range).
+template <int CG>
 struct FwdSched {
   int n_tiles, v_tiles, gN, S, num_kb;
-  int n_off, split;
+  int n_off, split, rank;
   int g, vt, vt_end, range, n_tile;
   bool first;
 
-  __device__ explicit FwdSched(const FwdParams& p)
-      : n_tiles(p.n_tiles), v_tiles(p.v_tiles), gN(p.gN), S(p.S), num_kb(p.num_kb),
-        n_off(int(blockIdx.x) % p.gN), split(int(blockIdx.x) / p.gN), g(-1), vt(0), vt_end(0), range(0),
-        n_tile(0), first(false) {}
+  __device__ explicit FwdSched(const FwdParams& p) : n_tiles(p.n_tiles), v_tiles(p.v_tiles), gN(p.gN), S(p.S),
+                                                     num_kb(p.num_kb) {
+    const Pair pr = pair_id<CG>();
+    n_off = pr.cid % gN;
+    split = pr.cid / gN;
+    rank = pr.rank;
+    g = -1;
+    vt = vt_end = range = n_tile = 0;
+    first = false;
+  }
 
   __device__ bool next(Tile& t) {
     if (vt >= vt_end) {
@@ -79,7 +122,7 @@ struct FwdSched {
       if (vt >= vt_end) return false;  // S <= v_tiles on the host, so never taken
       first = true;
     }
-    t.a_row = n_tile * kBM;
+    t.a_row = n_tile * Geo<CG>::kTileRows + rank * kBM;
     t.b_row = vt * kBN;
     t.a_k0 = 0;
     t.b_k0 = 0;
@@ -93,34 +136,34 @@ struct FwdSched {
 };
 
 // Static round-robin walk for the backward GEMMs. Tile index i = major * minor_count + minor.
-//   WALK_GRAD: major = row tile of X (128 rows), minor = 256-column vocabulary tile of the band.
-//   WALK_DW  : major = 256-column vocabulary tile, minor = 128-row tile of D.
-//   WALK_DX  : major = row tile of the band (128 rows), minor = 256-column tile of D.
-template <int KIND>
+//   WALK_GRAD: major = row tile of X, minor = 256-column vocabulary tile of the band.
+//   WALK_DW  : major = 256-column vocabulary tile, minor = row tile of D.
+//   WALK_DX  : major = row tile of the band, minor = 256-column tile of D.
+// Row tiles are kBM * CG rows (this CTA takes rows rank*128 .. rank*128+127 of each).
+template <int CG, int KIND>
 struct WalkSched {
   WalkParams w;
-  int i;
-  __device__ explicit WalkSched(const WalkParams& p) : w(p), i(int(blockIdx.x)) {}
+  int i, step, rank;
+  __device__ explicit WalkSched(const WalkParams& p) : w(p) {
+    const Pair pr = pair_id<CG>();
+    i = pr.cid;
+    step = pr.nclusters;
+    rank = pr.rank;
+  }
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;
     const int major = i / w.tiles_minor;
     const int minor = i - major * w.tiles_minor;
-    if (KIND == WALK_GRAD) {
-      t.a_row = major * kBM;
-      t.b_row = w.b_row_off + minor * kBN;
-    } else if (KIND == WALK_DW) {
-      t.a_row = minor * kBM;
-      t.b_row = w.b_row_off + major * kBN;
-    } else {
-      t.a_row = major * kBM;
-      t.b_row = w.b_row_off + minor * kBN;
-    }
+    const int rows = (KIND == WALK_DW) ? minor : major;
+    const int cols = (KIND == WALK_DW) ? major : minor;
+    t.a_row = rows * Geo<CG>::kTileRows + rank * kBM;
+    t.b_row = w.b_row_off + cols * kBN;
     t.a_k0 = w.a_k0;
     t.b_k0 = w.b_k0;
     t.num_kb = w.num_kb;
     t.aux = 0;
     t.flags = TILE_FIRST | TILE_LAST;
-    i += int(gridDim.x);
+    i += step;
     return true;
   }
 };
@@ -129,97 +172,178 @@ struct WalkSched {
 // Shared memory and the two async roles
 // ---------------------------------------------------------------------------------
 struct Smem {
-  uint8_t* stage;      // kStages x (A 16 KB | B 32 KB), 1024-byte aligned
+  uint8_t* stage;      // STAGES x (A 16 KB | B 32/CG KB), 1024-byte aligned
+  int stage_bytes;
   uint8_t* staging;    // epilogue store boxes, 16 KB each
-  uint64_t* full;      // [kStages] TMA -> MMA
-  uint64_t* empty;     // [kStages] MMA -> TMA
-  uint64_t* tfull;     // [2] accumulator ready for the epilogue
-  uint64_t* tempty;    // [2] accumulator drained
+  uint64_t* full;      // [STAGES] TMA -> MMA (used in the leader)
+  uint64_t* empty;     // [STAGES] MMA -> TMA (each CTA)
+  uint64_t* tfull;     // [2] accumulator ready for the epilogue (each CTA)
+  uint64_t* tempty;    // [2] accumulator drained (used in the leader)
   uint64_t* drain;     // MMA completion on abort
   uint32_t* tmem_slot;
   volatile int* abort_flag;
   volatile int* epi_go;  // [2]
 };
 
-__device__ __forceinline__ Smem carve_smem(uint8_t* raw, int staging_bufs) {
+template <int CG, int STAGES, int STAGING>
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
   Smem s;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   s.stage = base;
-  s.staging = base + kStages * kStageBytes;
-  uint8_t* b = s.staging + staging_bufs * kStagingBytes;
+  s.stage_bytes = Geo<CG>::kStageBytesCta;
+  s.staging = base + STAGES * Geo<CG>::kStageBytesCta;
+  uint8_t* b = s.staging + STAGING * kStagingBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(b);
   s.full = bars;
-  s.empty = bars + kStages;
-  s.tfull = bars + 2 * kStages;
-  s.tempty = bars + 2 * kStages + 2;
-  s.drain = bars + 2 * kStages + 4;
-  uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  s.empty = bars + STAGES;
+  s.tfull = bars + 2 * STAGES;
+  s.tempty = bars + 2 * STAGES + 2;
+  s.drain = bars + 2 * STAGES + 4;
+  uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   s.tmem_slot = words;
   s.abort_flag = reinterpret_cast<volatile int*>(words + 1);
   s.epi_go = reinterpret_cast<volatile int*>(words + 2);
   return s;
 }
 
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUtensorMap* tma, const CUtensorMap* tmb,
-                                           uint64_t* bar, const Tile& t, int kb) {
-  const int ka = t.a_k0 + kb * kBK;
-  const int kbb = t.b_k0 + kb * kBK;
-  if (!A_MN) {
-    tma_load_2d(sa, tma, bar, ka, t.a_row);  // box {64 K, 128 rows}
-  } else {
-#pragma unroll
-    for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * 8192, tma, bar, t.a_row + 64 * j, ka);  // {64 M, 64 K}
+template <int CG, int STAGES>
+__device__ __forceinline__ void init_barriers(const Smem& s) {
+  for (int i = 0; i < STAGES; ++i) {
+    mbar_init(&s.full[i], 1);
+    mbar_init(&s.empty[i], 1);
   }
-  if (!B_MN) {
-    tma_load_2d(sb, tmb, bar, kbb, t.b_row);  // box {64 K, 256 rows}
-  } else {
-#pragma unroll
-    for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * 8192, tmb, bar, t.b_row + 64 * j, kbb);  // {64 N, 64 K}
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&s.tfull[i], 1);
+    mbar_init(&s.tempty[i], Geo<CG>::kTemptyCount);
+  }
+  mbar_init(s.drain, 1);
+  *s.abort_flag = 0;
+  s.epi_go[0] = 0;
+  s.epi_go[1] = 0;
+  fence_barrier_init();
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_setup(const Smem& s, int warp) {
+  if (warp == 1) {
+    if (CG == 1) {
+      tmem_alloc(s.tmem_slot, 512);
+      tmem_relinquish_alloc_permit();
+    } else {
+      tmem_alloc_pair(s.tmem_slot, 512);
+      tmem_relinquish_alloc_permit_pair();
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (CG == 2) cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after_sync();
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_teardown(uint32_t tmem_base, int warp) {
+  tc_fence_before_sync();
+  __syncthreads();
+  if (CG == 2) cluster_sync_all();  // no peer still signals this CTA's barriers or reads its TMEM
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    if (CG == 1)
+      tmem_dealloc(tmem_base, 512);
+    else
+      tmem_dealloc_pair(tmem_base, 512);
   }
 }
 
-template <bool A_MN, bool B_MN>
+template <int CG, bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUtensorMap* tma, const CUtensorMap* tmb,
+                                           uint64_t* bar_local, uint32_t bar_leader, const Tile& t, int kb,
+                                           int rank) {
+  const int ka = t.a_k0 + kb * kBK;
+  const int kbb = t.b_k0 + kb * kBK;
+  const int b0 = t.b_row + rank * Geo<CG>::kBRows;
+  auto load = [&](void* dst, const CUtensorMap* m, int x, int y) {
+    if (CG == 1)
+      tma_load_2d(dst, m, bar_local, x, y);
+    else
+      tma_load_2d_pair(dst, m, bar_leader, x, y);
+  };
+  if (!A_MN) {
+    load(sa, tma, ka, t.a_row);  // box {64 K, 128 rows}
+  } else {
+#pragma unroll
+    for (int j = 0; j < kBM / 64; ++j) load(sa + j * 8192, tma, t.a_row + 64 * j, ka);  // {64 M, 64 K}
+  }
+  if (!B_MN) {
+    load(sb, tmb, kbb, b0);  // box {64 K, 256/CG rows}
+  } else {
+#pragma unroll
+    for (int j = 0; j < Geo<CG>::kBRows / 64; ++j) load(sb + j * 8192, tmb, b0 + 64 * j, kbb);  // {64 N, 64 K}
+  }
+}
+
+template <int CG, bool A_MN, bool B_MN>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sa, uint32_t sb, bool acc_first) {
-  constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, A_MN, B_MN);
+  constexpr uint32_t idesc = make_idesc_bf16(kBM * CG, kBN, A_MN, B_MN);
 #pragma unroll
   for (int kk = 0; kk < kBK / 16; ++kk) {
     // K-major: advance 16 elements = 32 bytes inside the swizzled 128-byte row.
     // MN-major: advance 16 K-rows = 2048 bytes; MN chunks of 64 elements are 8 KB apart.
     const uint64_t ad = A_MN ? make_sdesc_sw128(sa + kk * 2048, 8192, 1024) : make_sdesc_sw128(sa + kk * 32, 16, 1024);
     const uint64_t bd = B_MN ? make_sdesc_sw128(sb + kk * 2048, 8192, 1024) : make_sdesc_sw128(sb + kk * 32, 16, 1024);
-    tc_mma_bf16(d_tmem, ad, bd, idesc, (acc_first || kk > 0) ? 1u : 0u);
+    const uint32_t acc = (acc_first || kk > 0) ? 1u : 0u;
+    if (CG == 1)
+      tc_mma_bf16(d_tmem, ad, bd, idesc, acc);
+    else
+      tc_mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
   }
 }
 
-template <bool A_MN, bool B_MN, class Sched, class SP>
+template <int CG>
+__device__ __forceinline__ void commit_both(uint64_t* bar) {
+  if (CG == 1)
+    tc_commit(bar);
+  else
+    tc_commit_pair_multicast(bar, uint16_t(0x3));
+}
+
+template <int CG, int STAGES, bool A_MN, bool B_MN, class Sched, class SP>
 __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* tma, const CUtensorMap* tmb,
-                                              const SP& sp, const WaitCtx& w) {
+                                              const SP& sp, const WaitCtx& w, int rank) {
   Sched sched(sp);
   Tile t;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0, last_parity = 0;
   bool ok = true;
+  const bool leader = rank == 0;
   while (ok && sched.next(t)) {
     for (int kb = 0; kb < t.num_kb; ++kb) {
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, w)) { ok = false; break; }
-      mbar_arrive_expect_tx(&s.full[stage], kStageBytes);
-      uint8_t* sa = s.stage + stage * kStageBytes;
-      load_stage<A_MN, B_MN>(sa, sa + kABytes, tma, tmb, &s.full[stage], t, kb);
+      if (leader) mbar_arrive_expect_tx(&s.full[stage], Geo<CG>::kTxBytes);
+      uint8_t* sa = s.stage + stage * Geo<CG>::kStageBytesCta;
+      const uint32_t bar_leader = CG == 1 ? 0u : map_shared_to_rank(smem_addr(&s.full[stage]), 0);
+      load_stage<CG, A_MN, B_MN>(sa, sa + kABytes, tma, tmb, &s.full[stage], bar_leader, t, kb, rank);
       issued |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
   }
   if (!ok) {
-    // Aborting: let every copy this thread started land before the CTA exits.
-    for (int st = 0; st < kStages; ++st)
-      if (issued & (1u << st)) mbar_wait_drain(&s.full[st], (last_parity >> st) & 1u);
+    if (leader) {
+      // Aborting: let every copy landing on this CTA's barriers arrive before exit.
+      for (int st = 0; st < STAGES; ++st)
+        if (issued & (1u << st)) mbar_wait_drain(&s.full[st], (last_parity >> st) & 1u);
+    } else {
+      // The peer's copies complete on the leader's barriers: give them a bounded 1 ms.
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < 1000000ull) {
+      }
+    }
   }
 }
 
-template <bool A_MN, bool B_MN, class Sched, class SP>
+template <int CG, int STAGES, bool A_MN, bool B_MN, class Sched, class SP>
 __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, const SP& sp, const WaitCtx& w) {
   Sched sched(sp);
   Tile t;
@@ -236,20 +360,23 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
     for (int kb = 0; kb < t.num_kb; ++kb) {
       if (!mbar_wait(&s.full[stage], phase, w)) { ok = false; break; }
       tc_fence_after_sync();
-      const uint32_t sa = smem_addr(s.stage + stage * kStageBytes);
-      mma_stage<A_MN, B_MN>(d_tmem, sa, sa + kABytes, kb > 0);
+      const uint32_t sa = smem_addr(s.stage + stage * Geo<CG>::kStageBytesCta);
+      mma_stage<CG, A_MN, B_MN>(d_tmem, sa, sa + kABytes, kb > 0);
       issued_any = true;
-      tc_commit(&s.empty[stage]);
-      if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      commit_both<CG>(&s.empty[stage]);
+      if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    tc_commit(&s.tfull[acc]);
+    commit_both<CG>(&s.tfull[acc]);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
   if (!ok && issued_any) {
     // Aborting: wait for the MMAs already issued before TMEM is released.
-    tc_commit(s.drain);
+    if (CG == 1)
+      tc_commit(s.drain);
+    else
+      tc_commit_pair(s.drain);
     mbar_wait_drain(s.drain, 0);
   }
 }
@@ -269,9 +396,16 @@ __device__ __forceinline__ bool epi_acquire(const Smem& s, int acc, uint32_t acc
   return go;
 }
 
+// This thread has finished reading accumulator `acc` (all its tcgen05.ld waited on).
+template <int CG>
 __device__ __forceinline__ void epi_release(const Smem& s, int acc) {
   tc_fence_before_sync();
-  mbar_arrive(&s.tempty[acc]);
+  if (CG == 1) {
+    mbar_arrive(&s.tempty[acc]);
+  } else {
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive_cluster(map_shared_to_rank(smem_addr(&s.tempty[acc]), 0));
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -330,52 +464,34 @@ __device__ __forceinline__ void online_update(RowStats& st, const uint32_t (&r)[
   }
 }
 
+template <int CG, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_forward_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  const Smem s = carve_smem(smem_raw, 0);
+  const Smem s = carve_smem<CG, STAGES, 0>(smem_raw);
   const int warp = int(threadIdx.x) >> 5;
   const uint32_t lane = lane_id();
+  const int rank = pair_id<CG>().rank;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], kEpiThreads);
-    }
-    mbar_init(s.drain, 1);
-    *s.abort_flag = 0;
-    s.epi_go[0] = 0;
-    s.epi_go[1] = 0;
-    fence_barrier_init();
-  }
+  if (threadIdx.x == 0) init_barriers<CG, STAGES>(s);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) {
-    tmem_alloc(s.tmem_slot, 512);
-    tmem_relinquish_alloc_permit();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
+  tmem_setup<CG>(s, warp);
   const uint32_t tmem_base = *s.tmem_slot;
   const WaitCtx w{s.abort_flag, p.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<false, true, FwdSched>(s, &tmA, &tmB, p, w);
+    if (lane == 0) producer_role<CG, STAGES, false, true, FwdSched<CG>>(s, &tmA, &tmB, p, w, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<false, true, FwdSched>(s, tmem_base, p, w);
+    if (lane == 0 && rank == 0) mma_role<CG, STAGES, false, true, FwdSched<CG>>(s, tmem_base, p, w);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
     const uint32_t lane_addr = tmem_base + (uint32_t(32 * (warp & 3)) << 16);
-    FwdSched sched(p);
+    FwdSched<CG> sched(p);
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -397,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(taddr + uint32_t(c), r0);
         tmem_ld_32cols(taddr + uint32_t(c + 32), r1);
         tc_wait_ld();
-        if (c + 64 == kBN) epi_release(s, acc);
+        if (c + 64 == kBN) epi_release<CG>(s, acc);
         const int col0 = t.b_row + c;
         if (!tail_tile) {
           online_update<false>(st, r0, col0, p.V, y, want_sum);
@@ -418,14 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 512);
-  }
+  tmem_teardown<CG>(tmem_base, warp);
 }
 
 // ---------------------------------------------------------------------------------
@@ -460,56 +569,37 @@ __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32
   }
 }
 
-template <bool A_MN, bool B_MN, int KIND, int EPI>
+template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_walk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const WalkParams wp, const GradEpiParams gp,
                           const StoreEpiParams sp) {
   extern __shared__ uint8_t smem_raw[];
-  const Smem s = carve_smem(smem_raw, 2);
+  const Smem s = carve_smem<CG, STAGES, 2>(smem_raw);
   const int warp = int(threadIdx.x) >> 5;
   const uint32_t lane = lane_id();
+  const int rank = pair_id<CG>().rank;
   int* err = (EPI == 0) ? gp.err : sp.err;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s.full[i], 1);
-      mbar_init(&s.empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], kEpiThreads);
-    }
-    mbar_init(s.drain, 1);
-    *s.abort_flag = 0;
-    s.epi_go[0] = 0;
-    s.epi_go[1] = 0;
-    fence_barrier_init();
-  }
+  if (threadIdx.x == 0) init_barriers<CG, STAGES>(s);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
   }
-  if (warp == 1) {
-    tmem_alloc(s.tmem_slot, 512);
-    tmem_relinquish_alloc_permit();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
+  tmem_setup<CG>(s, warp);
   const uint32_t tmem_base = *s.tmem_slot;
   const WaitCtx w{s.abort_flag, err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<A_MN, B_MN, WalkSched<KIND>>(s, &tmA, &tmB, wp, w);
+    if (lane == 0) producer_role<CG, STAGES, A_MN, B_MN, WalkSched<CG, KIND>>(s, &tmA, &tmB, wp, w, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<A_MN, B_MN, WalkSched<KIND>>(s, tmem_base, wp, w);
+    if (lane == 0 && rank == 0) mma_role<CG, STAGES, A_MN, B_MN, WalkSched<CG, KIND>>(s, tmem_base, wp, w);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);
     const uint32_t lane_addr = tmem_base + (uint32_t(32 * (warp & 3)) << 16);
-    WalkSched<KIND> sched(wp);
+    WalkSched<CG, KIND> sched(wp);
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -530,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(taddr + uint32_t(c), r0);
           tmem_ld_32cols(taddr + uint32_t(c + 32), r1);
           tc_wait_ld();
-          if (c + 64 == kBN) epi_release(s, acc);
+          if (c + 64 == kBN) epi_release<CG>(s, acc);
           const int col0 = t.b_row + c;  // global vocabulary column
           uint4 chunks[8];
           uint32_t* packed = reinterpret_cast<uint32_t*>(chunks);
@@ -558,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r0[32];
           tmem_ld_32cols(taddr + uint32_t(c), r0);
           tc_wait_ld();
-          if (c + 32 == kBN) epi_release(s, acc);
+          if (c + 32 == kBN) epi_release<CG>(s, acc);
           uint4 chunks[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
@@ -572,232 +662,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (epi_tid == 0) bulk_wait_group<0>();  // every store has landed before the CTA exits
   }
-
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 512);
-  }
-}
-
-// ---------------------------------------------------------------------------------
-// Small kernels: forward finalize, backward row coefficients, dX cast
-// ---------------------------------------------------------------------------------
-
-// Combine the S partial statistics of each row into lse, form the row loss and
-// reduce it deterministically (per-block fp64 partial sums, then one block).
-__global__ void __launch_bounds__(kFinalizeThreads)
-    flce_finalize_rows_kernel(const FinalizeParams p) {
-  const int row = int(blockIdx.x) * kFinalizeThreads + int(threadIdx.x);
-  double contrib = 0.0;
-  int valid = 0;
-  if (row < p.N) {
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.part_m[size_t(s) * p.N + row]);
-    float d = 0.f, sz = 0.f;
-    for (int s = 0; s < p.S; ++s) {
-      const size_t o = size_t(s) * p.N + row;
-      d += p.part_d[o] * exp2f((p.part_m[o] - M) * kLog2e);
-      sz += p.part_s[o];
-    }
-    const float lse = M + logf(d);
-    p.lse[row] = lse;
-    const int y = p.targets[row];
-    float ell = 0.f;
-    if (y != p.ignore_index) {
-      valid = 1;
-      if (y < 0 || y >= p.V) {
-        atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
-        ell = CUDART_NAN_F;
-      } else {
-        const float zy = p.tgt[row];
-        ell = (1.f - p.eps) * (lse - zy) + p.zscale * lse * lse;
-        if (p.eps != 0.f) ell += p.eps * (lse - sz / float(p.V));
-      }
-    }
-    if (p.reduction == 2) p.loss[row] = ell;
-    contrib = double(ell);
-  }
-  if (p.reduction == 2) return;
-  // fixed-order block reduction
-  __shared__ double ssum[kFinalizeThreads];
-  __shared__ int scnt[kFinalizeThreads];
-  ssum[threadIdx.x] = contrib;
-  scnt[threadIdx.x] = valid;
-  __syncthreads();
-  for (int o = kFinalizeThreads / 2; o > 0; o >>= 1) {
-    if (int(threadIdx.x) < o) {
-      ssum[threadIdx.x] += ssum[threadIdx.x + o];
-      scnt[threadIdx.x] += scnt[threadIdx.x + o];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    p.block_sum[blockIdx.x] = ssum[0];
-    p.block_cnt[blockIdx.x] = scnt[0];
-  }
-}
-
-__global__ void __launch_bounds__(kFinalizeThreads)
-    flce_finalize_loss_kernel(const FinalizeParams p, int blocks) {
-  __shared__ double ssum[kFinalizeThreads];
-  __shared__ long long scnt[kFinalizeThreads];
-  double s = 0.0;
-  long long c = 0;
-  for (int b = int(threadIdx.x); b < blocks; b += kFinalizeThreads) {
-    s += p.block_sum[b];
-    c += p.block_cnt[b];
-  }
-  ssum[threadIdx.x] = s;
-  scnt[threadIdx.x] = c;
-  __syncthreads();
-  for (int o = kFinalizeThreads / 2; o > 0; o >>= 1) {
-    if (int(threadIdx.x) < o) {
-      ssum[threadIdx.x] += ssum[threadIdx.x + o];
-      scnt[threadIdx.x] += scnt[threadIdx.x + o];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    double total = ssum[0];
-    if (p.reduction == 0) total = scnt[0] ? total / double(scnt[0]) : 0.0;
-    p.loss[0] = float(total);
-  }
-}
-
-// One block: count valid rows (16-byte vector loads of the targets), form g, then the
-// per-row coefficients {a = g(1 + 2 s lse), -lse log2e, b = g eps / V, target} the
-// gradient epilogue reads with one 16-byte load per row.
-constexpr int kPrepThreads = 1024;
-
-__global__ void __launch_bounds__(kPrepThreads) flce_prep_kernel(const PrepParams p) {
-  __shared__ int s_cnt[kPrepThreads / 32];
-  __shared__ float s_g;
-  const int tid = int(threadIdx.x);
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(p.targets);
-  const flce_vec_split sp = flce_split_for_vectors(int64_t((addr & 15u) / 4u), p.N, 4);
-  int cnt = 0;
-  for (int64_t i = tid; i < sp.head; i += kPrepThreads) cnt += (p.targets[i] != p.ignore_index);
-  const int4* body = reinterpret_cast<const int4*>(p.targets + sp.head);
-  for (int64_t i = tid; i < sp.body / 4; i += kPrepThreads) {
-    const int4 v = __ldg(body + i);
-    cnt += (v.x != p.ignore_index) + (v.y != p.ignore_index) + (v.z != p.ignore_index) + (v.w != p.ignore_index);
-  }
-  for (int64_t i = sp.head + sp.body + tid; i < p.N; i += kPrepThreads) cnt += (p.targets[i] != p.ignore_index);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if ((tid & 31) == 0) s_cnt[tid >> 5] = cnt;
-  __syncthreads();
-  if (tid < 32) {
-    int c = s_cnt[tid];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (tid == 0) {
-      float g = *p.grad_out;
-      if (p.reduction == 0) g = c ? g / float(c) : 0.f;
-      s_g = g;
-      *p.cval = g * (1.f - p.eps);
-    }
-  }
-  __syncthreads();
-  const float g = s_g;
-  const float b = g * p.eps / float(p.V);
-  for (int i = tid; i < p.N; i += kPrepThreads) {
-    const int y = p.targets[i];
-    float4 cf;
-    if (y == p.ignore_index) {
-      cf = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
-    } else if (y < 0 || y >= p.V) {
-      atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
-      cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(-1));
-    } else {
-      const float l = p.lse[i];
-      cf = make_float4(g * (1.f + 2.f * p.zscale * l), -l * kLog2e, b, __int_as_float(y));
-    }
-    p.coef[i] = cf;
-  }
-}
-
-__global__ void flce_cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
-  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
-    const float4 v = src[i];
-    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-  }
+  tmem_teardown<CG>(tmem_base, warp);
 }
 
 // ---------------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------------
-template <class K>
-static cudaError_t set_smem(K kernel, size_t bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+namespace {
+
+constexpr int kCG = 2;           // CTA pair (cta_group::2) for every GEMM
+constexpr int kFwdStages = 7;    // 7 x 32 KB
+constexpr int kWalkStages = 6;   // 6 x 32 KB + 2 x 16 KB epilogue boxes
+
+template <class Kern>
+cudaError_t prepare(Kern kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
 }
+
+cudaLaunchConfig_t make_config(int grid, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters that can be resident at once (cached per device and kernel kind).
+template <class Kern>
+int max_clusters(Kern kernel, size_t smem, int slot) {
+  static int cache[64][4];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev][slot] > 0) return cache[dev][slot];
+  if (prepare(kernel, smem) != cudaSuccess) return 0;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config(sms - sms % kCG, smem, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / kCG;
+  }
+  cache[dev][slot] = n;
+  return n;
+}
+
+auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kFwdStages>; }
+auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, true, WALK_GRAD, 0>; }
+auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, true, true, WALK_DW, 1>; }
+auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, false, WALK_DX, 1>; }
+
+constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
+constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
+static_assert(kFwdSmem <= 232448 && kWalkSmem <= 232448, "shared memory per CTA");
+
+template <class Kern>
+cudaError_t launch_walk(Kern kernel, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                        const WalkParams& w, const GradEpiParams& g, const StoreEpiParams& s, int slot,
+                        cudaStream_t stream) {
+  cudaError_t e = prepare(kernel, kWalkSmem);
+  if (e != cudaSuccess) return e;
+  const int maxc = max_clusters(kernel, kWalkSmem, slot);
+  if (maxc <= 0) return cudaErrorInvalidConfiguration;
+  const int clusters = w.total_tiles < maxc ? w.total_tiles : maxc;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config(clusters * kCG, kWalkSmem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, w, g, s);
+}
+
+}  // namespace
+
+int gemm_tile_rows() { return kBM * kCG; }
+
+int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
+
+int forward_max_units() { return max_clusters(fwd_kernel(), kFwdSmem, 0); }
 
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p,
                                 cudaStream_t stream) {
-  const size_t smem = gemm_smem_bytes(0);
-  cudaError_t e = set_smem(flce_forward_gemm_kernel, smem);
+  auto kern = fwd_kernel();
+  cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
-  flce_forward_gemm_kernel<<<p.gN * p.S, kThreads, smem, stream>>>(tmA, tmB, p);
-  return cudaGetLastError();
-}
-
-template <bool A_MN, bool B_MN, int KIND, int EPI>
-static cudaError_t launch_walk(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                               const WalkParams& w, const GradEpiParams& g, const StoreEpiParams& s, int grid,
-                               cudaStream_t stream) {
-  auto kern = flce_walk_gemm_kernel<A_MN, B_MN, KIND, EPI>;
-  const size_t smem = gemm_smem_bytes(2);
-  cudaError_t e = set_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(tmA, tmB, tmC, w, g, s);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_config(p.gN * p.S * kCG, kFwdSmem, stream, attr);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, int grid, cudaStream_t stream) {
+                             const WalkParams& w, const GradEpiParams& e, cudaStream_t stream) {
   StoreEpiParams unused{0, 0, e.err};
-  return launch_walk<false, true, WALK_GRAD, 0>(tmA, tmB, tmC, w, e, unused, grid, stream);
+  return launch_walk(grad_kernel(), tmA, tmB, tmC, w, e, unused, 1, stream);
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, int grid, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
   GradEpiParams unused{nullptr, nullptr, 0, 0, 0, e.err};
-  return launch_walk<true, true, WALK_DW, 1>(tmA, tmB, tmC, w, unused, e, grid, stream);
+  return launch_walk(dw_kernel(), tmA, tmB, tmC, w, unused, e, 2, stream);
 }
 
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, int grid, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
   GradEpiParams unused{nullptr, nullptr, 0, 0, 0, e.err};
-  return launch_walk<false, false, WALK_DX, 1>(tmA, tmB, tmC, w, unused, e, grid, stream);
-}
-
-cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream) {
-  flce_finalize_rows_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.reduction == 2) return e;
-  flce_finalize_loss_kernel<<<1, kFinalizeThreads, 0, stream>>>(p, blocks);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
-  flce_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, int num_sms, cudaStream_t stream) {
-  const size_t n4 = n / 4;
-  size_t blocks = (n4 + 255) / 256;
-  const size_t cap = size_t(num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks == 0) blocks = 1;
-  flce_cast_bf16_kernel<<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
-                                                              reinterpret_cast<uint2*>(dst), n4);
-  return cudaGetLastError();
+  return launch_walk(dx_kernel(), tmA, tmB, tmC, w, unused, e, 3, stream);
 }
 
 }  // namespace flce

@@ -14,27 +14,21 @@ namespace flce {
 constexpr int FLCE_DEVERR_BAD_TARGET = 1;
 constexpr int FLCE_DEVERR_TIMEOUT = 2;
 
-// Output tile of every tensor-core GEMM: 128 rows (TMEM lanes) x 256 columns,
-// K staged 64 bf16 (128 bytes, one 128B-swizzle row) at a time.
+// Output tiles of the tensor-core GEMMs: 128 rows per CTA (TMEM lanes) x 256 columns,
+// a CTA pair (cluster of 2) owning 256 x 256; K staged 64 bf16 (128 bytes, one
+// 128B-swizzle row) at a time.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;      // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kEpiThreads = 128;
-constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kStagingBytes = 128 * 128;        // one 128-row x 128-byte epilogue store box
 constexpr int kBarrierBytes = 256;
 
 // Forward split of the vocabulary: at most this many partial (max, sum-exp, sum-z)
 // triples per row.
 constexpr int kMaxSplits = 64;
-
-constexpr size_t gemm_smem_bytes(int staging_bufs) {
-  return size_t(kStages) * kStageBytes + size_t(staging_bufs) * kStagingBytes + kBarrierBytes + 1024;
-}
 
 // Tile walk of the non-forward GEMMs; see the kernel for how a tile index maps to
 // operand rows.
@@ -52,7 +46,7 @@ struct FwdParams {
   const int32_t* targets;
   int N, V;
   int n_tiles, v_tiles;
-  int gN, S;       // CTA grid = gN row tiles x S vocabulary ranges
+  int gN, S;       // grid = gN row tiles x S vocabulary ranges (CTA pairs)
   int num_kb;      // K blocks over D
   int want_sum_z;  // label smoothing needs sum_j z_ij
   float* part_m;   // [S][N] running max
@@ -106,16 +100,24 @@ struct PrepParams {
   int* err;
 };
 
+// Rows of one GEMM output tile (a CTA pair: 2 x 128).
+int gemm_tile_rows();
+// Rows (K-major) or columns (MN-major) of the B operand each CTA loads: 256 / pair size.
+int gemm_b_rows_per_cta();
+// CTA pairs of the forward GEMM that can be resident at once on the current device.
+int forward_max_units();
+
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p,
                                 cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+// The walk GEMMs size their own grids: min(tiles, resident CTA pairs) clusters of 2.
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, int grid, cudaStream_t stream);
+                             const WalkParams& w, const GradEpiParams& e, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, int grid, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, int grid, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, int num_sms, cudaStream_t stream);
 
 constexpr int kFinalizeThreads = 256;

@@ -27,8 +27,19 @@ using namespace flce;
 
 namespace {
 
+// Compile-time tunables (defaults are the measured choices).
+#ifndef FLCE_BAND_BYTES
+#define FLCE_BAND_BYTES (int64_t(1) << 30)  // byte budget of the bf16 gradient band
+#endif
+#ifndef FLCE_BAND_W_L2_BYTES
+#define FLCE_BAND_W_L2_BYTES int64_t(0)  // if > 0: also cap the band so its W slice (2*D*Vc) fits this
+#endif
+#ifndef FLCE_FWD_GN
+#define FLCE_FWD_GN 0  // forward row tiles per group; 0 chooses from the resident CTA pairs
+#endif
+
 constexpr size_t kHeaderBytes = 256;
-constexpr int64_t kGradBandBudget = int64_t(1) << 30;  // bytes of bf16 gradient band
+constexpr int64_t kGradBandBudget = FLCE_BAND_BYTES;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -63,8 +74,12 @@ struct BwdLayout {
 // Width of the gradient band: as many 256-column tiles as fit in the byte budget,
 // and never more than half the vocabulary (rounded up to a tile), so that no buffer
 // holds N x V values once V exceeds one tile.
-int64_t band_width(int64_t N, int64_t V) {
+int64_t band_width(int64_t N, int64_t D, int64_t V) {
   int64_t vc = (kGradBandBudget / (2 * N)) / kBN * kBN;
+  if (FLCE_BAND_W_L2_BYTES > 0) {
+    const int64_t l2 = (FLCE_BAND_W_L2_BYTES / (2 * D)) / kBN * kBN;
+    if (l2 < vc) vc = l2;
+  }
   if (vc < kBN) vc = kBN;
   const int64_t half = cdiv(cdiv(V, 2), kBN) * kBN;
   if (vc > half) vc = half;
@@ -73,7 +88,7 @@ int64_t band_width(int64_t N, int64_t V) {
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   BwdLayout L{};
-  L.Vc = band_width(N, V);
+  L.Vc = band_width(N, D, V);
   size_t o = kHeaderBytes;
   L.coef = o; o += align256(size_t(N) * 16);
   L.band = o; o += align256(size_t(N) * size_t(L.Vc) * 2);
@@ -170,6 +185,7 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
       gN = c;
       break;
     }
+  if (FLCE_FWD_GN > 0 && FLCE_FWD_GN <= units) gN = FLCE_FWD_GN;
   if (gN > n_tiles) gN = int(n_tiles);
   int64_t S = units / gN;
   if (S > v_tiles) S = v_tiles;

@@ -50,7 +50,8 @@ import numpy as np
 __all__ = [
     "widen", "logits", "logsumexp_rows", "row_losses", "reduce_loss", "grad_scale",
     "grad_logits", "forward", "backward", "forward_backward", "full_row_stats",
-    "grad_x_rows", "grad_w_cols", "REDUCTIONS",
+    "grad_x_rows", "grad_w_cols", "REDUCTIONS", "ext_logits", "ext_row_losses", "ext_denominator",
+    "ext_grad_u", "argmax_first", "forward_ext", "forward_backward_ext", "shard_stats", "combine_shard_stats",
 ]
 
 REDUCTIONS = ("mean", "sum", "none")
@@ -285,3 +286,165 @@ def grad_w_cols(X, W, y, cols, lse: np.ndarray, g: float, ignore_index: int = -1
                          zloss_scale, g, cols=cols)
         out += Xb.T @ dz
     return out
+
+
+# ---------------------------------------------------------------------------
+# Extended options (Liger-Kernel PR #1291 "Summary" feature list): logit
+# softcap, a vocabulary bias, per-class weights, argmax metrics, and the
+# vocabulary-parallel split of the reduction. The pages name these features
+# without defining them; the readings below are torch's conventions (the PR
+# claims parity with torch) and are listed in the design notes.
+# ---------------------------------------------------------------------------
+
+def ext_logits(X: np.ndarray, W: np.ndarray, bias=None, softcap: float = 0.0):
+    """(z, u): z = X @ W (+ bias broadcast over rows); u = softcap * tanh(z / softcap) if softcap > 0."""
+    z = logits(X, W)
+    if bias is not None:
+        z = z + widen(bias)[None, :]
+    if softcap and softcap > 0:
+        u = float(softcap) * np.tanh(z / float(softcap))
+    else:
+        u = z
+    return z, u
+
+
+def ext_row_losses(u, lse, y, V, ignore_index, label_smoothing, zloss_scale, class_weight=None):
+    """l_i = (1-eps) w_{y_i} (lse_i - u_{i,y_i}) + (eps/V) sum_j w_j (lse_i - u_ij) + s lse_i^2.
+
+    torch's weighted, label-smoothed cross-entropy per row plus the z-loss; w = 1 gives
+    ``row_losses``. Ignored rows 0, out-of-range targets NaN.
+    """
+    y = _int_targets(y)
+    valid, bad = _valid_and_bad(y, V, ignore_index)
+    w = np.ones(V) if class_weight is None else widen(class_weight)
+    safe_y = np.where(valid & ~bad, y, 0)
+    u_y = u[np.arange(u.shape[0]), safe_y]
+    eps = float(label_smoothing)
+    smooth = (lse * w.sum() - u @ w) / V
+    ell = (1.0 - eps) * w[safe_y] * (lse - u_y) + eps * smooth + float(zloss_scale) * lse * lse
+    ell = np.where(valid, ell, 0.0)
+    return np.where(bad, np.nan, ell)
+
+
+def ext_denominator(y, V, ignore_index, class_weight=None) -> float:
+    """Mean denominator: the number of valid rows, or the sum of their target weights."""
+    y = _int_targets(y)
+    valid, bad = _valid_and_bad(y, V, ignore_index)
+    ok = valid & ~bad
+    if class_weight is None:
+        return float(valid.sum())
+    w = widen(class_weight)
+    return float(w[y[ok]].sum())
+
+
+def ext_grad_u(u, lse, y, V, ignore_index, label_smoothing, zloss_scale, g, class_weight=None):
+    """dU_ij = g [p_ij ((1-eps) w_y + (eps/V) W + 2 s lse_i) - (eps/V) w_j - (1-eps) w_y delta_{j,y}].
+
+    The gradient of ``ext_row_losses`` with respect to u (W = sum_j w_j); w = 1 gives
+    ``grad_logits``.
+    """
+    y = _int_targets(y)
+    valid, bad = _valid_and_bad(y, V, ignore_index)
+    w = np.ones(V) if class_weight is None else widen(class_weight)
+    eps = float(label_smoothing)
+    ok = valid & ~bad
+    safe_y = np.where(ok, y, 0)
+    wy = w[safe_y]
+    p = np.exp(u - lse[:, None])
+    a = (1.0 - eps) * wy + eps / V * w.sum() + 2.0 * float(zloss_scale) * lse
+    du = p * a[:, None] - (eps / V) * w[None, :]
+    rows = np.nonzero(ok)[0]
+    du[rows, y[rows]] -= (1.0 - eps) * wy[rows]
+    du *= g
+    du[~valid] = 0.0
+    du[bad] = np.nan
+    return du
+
+
+def argmax_first(u: np.ndarray) -> np.ndarray:
+    """Index of each row's largest value, the smallest such index on ties (torch.argmax)."""
+    return np.argmax(u, axis=1)
+
+
+def forward_ext(X, W, y, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",
+                softcap=0.0, bias=None, class_weight=None):
+    """Loss, lse, predicted [N] and accuracy of the extended options.
+
+    accuracy = (valid rows whose argmax equals the target) / (valid rows), 0 if none.
+    """
+    X, W = widen(X), widen(W)
+    y = _int_targets(y)
+    V = W.shape[1]
+    _, u = ext_logits(X, W, bias, softcap)
+    lse = logsumexp_rows(u)
+    ell = ext_row_losses(u, lse, y, V, ignore_index, label_smoothing, zloss_scale, class_weight)
+    valid, _ = _valid_and_bad(y, V, ignore_index)
+    if reduction == "none":
+        loss = ell
+    elif reduction == "sum":
+        loss = float(ell.sum())
+    else:
+        den = ext_denominator(y, V, ignore_index, class_weight)
+        loss = float(ell.sum()) / den if den else 0.0
+    pred = argmax_first(u)
+    n_valid = int(valid.sum())
+    acc = float((pred[valid] == y[valid]).sum()) / n_valid if n_valid else 0.0
+    return loss, lse, pred, acc
+
+
+def forward_backward_ext(X, W, y, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",
+                         grad_out=1.0, softcap=0.0, bias=None, class_weight=None):
+    """Loss, lse, dX, dW, dbias of the extended options (dbias None without a bias).
+
+    dZ = dU * (1 - (u / softcap)^2) with a softcap (the derivative of c tanh(z / c)),
+    dX = dZ W^T, dW = X^T dZ, dbias = sum over rows of dZ.
+    """
+    X, W = widen(X), widen(W)
+    y = _int_targets(y)
+    V = W.shape[1]
+    z, u = ext_logits(X, W, bias, softcap)
+    lse = logsumexp_rows(u)
+    loss = forward_ext(X, W, y, ignore_index, label_smoothing, zloss_scale, reduction, softcap, bias,
+                       class_weight)[0]
+    if reduction == "sum":
+        g = float(grad_out)
+    elif reduction == "mean":
+        den = ext_denominator(y, V, ignore_index, class_weight)
+        g = float(grad_out) / den if den else 0.0
+    else:
+        raise ValueError("the backward pass needs reduction 'mean' or 'sum'")
+    du = ext_grad_u(u, lse, y, V, ignore_index, label_smoothing, zloss_scale, g, class_weight)
+    dz = du * (1.0 - (u / float(softcap)) ** 2) if softcap and softcap > 0 else du
+    dbias = dz.sum(axis=0) if bias is not None else None
+    return loss, lse, dz @ W.T, X.T @ dz, dbias
+
+
+def shard_stats(X, W_shard, y, v_offset: int, ignore_index=-100):
+    """Per-row statistics of one vocabulary shard: (lse over the shard, sum of its logits,
+    target logit if the target falls in the shard else 0, 1.0 if it does else 0.0)."""
+    X, Ws = widen(X), widen(W_shard)
+    y = _int_targets(y)
+    z = logits(X, Ws)
+    lse_k = logsumexp_rows(z)
+    rel = y - int(v_offset)
+    own = (y != ignore_index) & (rel >= 0) & (rel < Ws.shape[1])
+    zy = np.where(own, z[np.arange(z.shape[0]), np.where(own, rel, 0)], 0.0)
+    return lse_k, z.sum(axis=1), zy, own.astype(np.float64)
+
+
+def combine_shard_stats(stats, V_total, y, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0,
+                        reduction="mean"):
+    """lse and loss from the shards' statistics: lse = log sum_k exp(lse_k), the target logit
+    and the logit sum are sums over shards; then the row loss of ``row_losses``."""
+    y = _int_targets(y)
+    lse_k = np.stack([s[0] for s in stats])
+    m = lse_k.max(axis=0)
+    lse = m + np.log(np.exp(lse_k - m[None, :]).sum(axis=0))
+    sum_z = sum(s[1] for s in stats)
+    zy = sum(s[2] for s in stats)
+    valid, bad = _valid_and_bad(y, V_total, ignore_index)
+    eps = float(label_smoothing)
+    ell = (1.0 - eps) * (lse - zy) + eps * (lse - sum_z / V_total) + float(zloss_scale) * lse * lse
+    ell = np.where(valid, ell, 0.0)
+    ell = np.where(bad, np.nan, ell)
+    return reduce_loss(ell, valid, reduction), lse

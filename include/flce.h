@@ -90,11 +90,11 @@ typedef enum {
   FLCE_REDUCTION_NONE = 2
 } flce_reduction;
 
-/* Bytes of workspace that flce_forward (for_backward == 0) or flce_backward
- * (for_backward != 0) needs for this shape on the current device. Returns 0 for
- * invalid sizes. The backward workspace holds a bf16 gradient band of N x Vc
- * columns (Vc < V, a multiple of 256) and an fp32 [N, D] dX accumulator; no
- * buffer has N x V elements. */
+/* Bytes of workspace that flce_forward (for_backward == 0), flce_backward
+ * (for_backward == 1) or flce_forward_backward (for_backward == 2) needs for this
+ * shape. Returns 0 for invalid sizes. The backward workspace holds a bf16 gradient
+ * band of N x Vc columns (Vc < V, a multiple of 256) and an fp32 [N, D] dX
+ * accumulator; no buffer has N x V elements. */
 size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward);
 
 /* Forward pass. [P1] "Definition and Forward Pass" and "Kernel Implementation"
@@ -129,6 +129,76 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
                           float label_smoothing, float zloss_scale, flce_reduction red,
                           const float* grad_out, void* dX, float* dW,
                           void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Optional features of the extended entry points below. [P4] "Summary" names them
+ * (softcap, bias, ce_weight, token accuracy, predicted tokens, vocabulary-parallel
+ * use through the Megatron path of [P3]) without defining them; the semantics are
+ * torch's, as [P4] claims parity with torch:
+ *   z_ij = sum_k X_ik W_kj + bias_j,   u_ij = softcap * tanh(z_ij / softcap) (softcap > 0) else z_ij,
+ *   l_i  = (1-eps) w_{y_i} (lse_i - u_{i,y_i}) + (eps/V) sum_j w_j (lse_i - u_ij) + s lse_i^2,
+ *   MEAN divides by sum over valid rows of w_{y_i} (the valid-row count when w == 1),
+ *   dU_ij = g [p_ij ((1-eps) w_{y_i} + (eps/V) sum_j w_j + 2 s lse_i) - (eps/V) w_j - (1-eps) w_{y_i} delta],
+ *   dZ = dU (1 - (u/softcap)^2) with a softcap,  dbias = sum_i dZ_i,
+ *   predicted_i = argmax_j u_ij (smallest index on ties), accuracy = matches / valid rows.
+ * Zero-initialise the struct and set what you need; NULL means "no options". */
+typedef struct flce_options {
+  float softcap;             /* > 0: cap the logits with softcap*tanh(z/softcap); 0: off */
+  const float* bias;         /* device fp32 [V] added to every row's logits, or NULL */
+  const float* class_weight; /* device fp32 [V] per-class weights (all >= 0), or NULL */
+  int32_t* predicted;        /* forward out: device int32 [N] argmax of each row, or NULL */
+  float* accuracy;           /* forward out: device fp32 [1] argmax == target over valid rows, or NULL */
+  float* dbias;              /* backward out: device fp32 [V] (needs bias), or NULL */
+  float* dX_f32;             /* backward out: device fp32 [N, D] dX written instead of the bf16 dX, or NULL */
+  int64_t v_offset;          /* vocabulary shard: global index of W's first column (0 if unsharded) */
+  int64_t v_total;           /* vocabulary shard: size of the full vocabulary (0 means V: unsharded) */
+} flce_options;
+
+/* flce_forward with options (NULL behaves exactly like flce_forward). Vocabulary
+ * shards (v_total > V) are not accepted here: use flce_shard_stats. */
+flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets,
+                            int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                            float label_smoothing, float zloss_scale, flce_reduction red,
+                            const flce_options* opt, float* loss, float* lse,
+                            void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* flce_backward with options. With opt->v_total > V, W holds the columns
+ * [v_offset, v_offset + V) of a vocabulary of v_total, lse is the full-vocabulary
+ * log-sum-exp (flce_combine_shards), dW is this shard's [D, V] block and dX (or dX_f32)
+ * this shard's partial dX, to be summed over shards by the caller (e.g. an
+ * all-reduce). Shards support label smoothing and z-loss, not the other options. */
+flce_status flce_backward_ex(const void* X, const void* W, const int32_t* targets, const float* lse,
+                             int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                             float label_smoothing, float zloss_scale, flce_reduction red,
+                             const flce_options* opt, const float* grad_out, void* dX, float* dW,
+                             void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Forward and backward in one call, for a loss that is the last layer ([P1] "Kernel
+ * Implementation" fuses both passes for that reason). Same outputs as flce_forward_ex
+ * followed by flce_backward_ex; workspace: flce_workspace_size(N, D, V, 2) bytes. */
+flce_status flce_forward_backward(const void* X, const void* W, const int32_t* targets,
+                                  int64_t N, int64_t D, int64_t V, int32_t ignore_index,
+                                  float label_smoothing, float zloss_scale, flce_reduction red,
+                                  const flce_options* opt, const float* grad_out,
+                                  float* loss, float* lse, void* dX, float* dW,
+                                  void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Vocabulary-parallel forward, one shard: W holds columns [v_offset, v_offset + V)
+ * of the full vocabulary. Writes stats, device fp32 [4][N]: the shard's log-sum-exp,
+ * the sum of the shard's logits, the target logit if the target is in the shard
+ * (else 0) and 1/0 for whether it is. Gather the shards' stats (e.g. all-gather,
+ * 16 bytes per row per shard) and call flce_combine_shards. Workspace:
+ * flce_workspace_size(N, D, V, 0). */
+flce_status flce_shard_stats(const void* X, const void* W, const int32_t* targets,
+                             int64_t N, int64_t D, int64_t V, int64_t v_offset, int32_t ignore_index,
+                             float* stats, void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
+/* Combine K shards' stats (device fp32 [K][4][N], shard order irrelevant) into the
+ * full-vocabulary lse [N] and the loss, as flce_forward would for the whole
+ * vocabulary of v_total classes. Workspace: flce_workspace_size(N, 8, 8, 0). */
+flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* targets, int64_t N,
+                                int64_t v_total, int32_t ignore_index, float label_smoothing,
+                                float zloss_scale, flce_reduction red, float* loss, float* lse,
+                                void* workspace, size_t ws_bytes, struct CUstream_st* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
  * most recent call that used `workspace`. Returns FLCE_OK, FLCE_ERR_BAD_TARGET,

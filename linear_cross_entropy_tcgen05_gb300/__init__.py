@@ -19,7 +19,9 @@ import torch
 __all__ = [
     "FLCEError", "load_library", "library_path", "flce_workspace_size", "flce_forward", "flce_backward",
     "flce_check_device_error", "flce_status_string", "flce_version", "linear_cross_entropy",
-    "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS",
+    "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
+    "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
+    "flce_combine_shards",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,7 +34,23 @@ STATUS = {
     7: "FLCE_ERR_BAD_TARGET", 8: "FLCE_ERR_TIMEOUT", 9: "FLCE_ERR_TOO_LARGE",
 }
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
-                    "flce_status_string", "flce_version", "flce_forward_noalloc")
+                    "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
+                    "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards")
+
+
+class FlceOptions(ctypes.Structure):
+    """Mirror of ``flce_options`` in include/flce.h."""
+
+    _fields_ = [("softcap", ctypes.c_float), ("bias", ctypes.c_void_p), ("class_weight", ctypes.c_void_p),
+                ("predicted", ctypes.c_void_p), ("accuracy", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
+                ("dX_f32", ctypes.c_void_p), ("v_offset", ctypes.c_int64), ("v_total", ctypes.c_int64)]
+
+
+def make_options(softcap: float = 0.0, bias=None, class_weight=None, predicted=None, accuracy=None, dbias=None,
+                 dX_f32=None, v_offset: int = 0, v_total: int = 0):
+    """An ``flce_options`` value (device tensors become pointers)."""
+    return FlceOptions(float(softcap), _ptr(bias), _ptr(class_weight), _ptr(predicted), _ptr(accuracy),
+                       _ptr(dbias), _ptr(dX_f32), int(v_offset), int(v_total))
 
 
 class FLCEError(RuntimeError):
@@ -69,6 +87,19 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_version.argtypes = []
     lib.flce_version.restype = ctypes.c_int
+    op = ctypes.POINTER(FlceOptions)
+    lib.flce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp, sz, vp]
+    lib.flce_forward_ex.restype = ctypes.c_int
+    lib.flce_backward_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp,
+                                     vp, sz, vp]
+    lib.flce_backward_ex.restype = ctypes.c_int
+    lib.flce_forward_backward.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp,
+                                          vp, vp, vp, sz, vp]
+    lib.flce_forward_backward.restype = ctypes.c_int
+    lib.flce_shard_stats.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz, vp]
+    lib.flce_shard_stats.restype = ctypes.c_int
+    lib.flce_combine_shards.argtypes = [vp, i32, vp, i64, i64, i32, f32, f32, ctypes.c_int, vp, vp, vp, sz, vp]
+    lib.flce_combine_shards.restype = ctypes.c_int
     if path is None:
         _LIB = lib
     return lib
@@ -144,6 +175,77 @@ def flce_backward(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_index:
         _nbytes(workspace) if ws_bytes is None else int(ws_bytes), _stream(stream))
     if raise_on_error:
         _check(st, "flce_backward")
+    return st
+
+
+def _red(reduction) -> int:
+    return REDUCTIONS[reduction] if isinstance(reduction, str) else int(reduction)
+
+
+def _opt_ref(options):
+    return ctypes.byref(options) if options is not None else None
+
+
+def flce_forward_ex(X, W, targets, loss, lse, workspace, ignore_index: int = -100, label_smoothing: float = 0.0,
+                    zloss_scale: float = 0.0, reduction: str = "mean", options: FlceOptions | None = None,
+                    stream=None, raise_on_error: bool = True) -> int:
+    """Call flce_forward_ex (``options`` from ``make_options``)."""
+    st = load_library().flce_forward_ex(
+        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(loss), _ptr(lse),
+        _ptr(workspace), _nbytes(workspace), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_forward_ex")
+    return st
+
+
+def flce_backward_ex(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_index: int = -100,
+                     label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean",
+                     options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
+    """Call flce_backward_ex (dX may be None when options.dX_f32 is set)."""
+    st = load_library().flce_backward_ex(
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(dX),
+        _ptr(dW), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_backward_ex")
+    return st
+
+
+def flce_forward_backward(X, W, targets, grad_out, loss, lse, dX, dW, workspace, ignore_index: int = -100,
+                          label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean",
+                          options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
+    """Call flce_forward_backward (workspace: flce_workspace_size(N, D, V, 2) bytes)."""
+    st = load_library().flce_forward_backward(
+        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(loss),
+        _ptr(lse), _ptr(dX), _ptr(dW), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_forward_backward")
+    return st
+
+
+def flce_shard_stats(X, W_shard, targets, v_offset: int, stats, workspace, ignore_index: int = -100, stream=None,
+                     raise_on_error: bool = True) -> int:
+    """Call flce_shard_stats: stats is a device fp32 [4, N] tensor."""
+    st = load_library().flce_shard_stats(
+        _ptr(X), _ptr(W_shard), _ptr(targets), X.shape[0], X.shape[1], W_shard.shape[1], int(v_offset),
+        int(ignore_index), _ptr(stats), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_shard_stats")
+    return st
+
+
+def flce_combine_shards(stats, targets, v_total: int, loss, lse, workspace, ignore_index: int = -100,
+                        label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean",
+                        stream=None, raise_on_error: bool = True) -> int:
+    """Call flce_combine_shards: stats is a device fp32 [K, 4, N] tensor."""
+    st = load_library().flce_combine_shards(
+        _ptr(stats), int(stats.shape[0]), _ptr(targets), int(stats.shape[2]), int(v_total), int(ignore_index),
+        float(label_smoothing), float(zloss_scale), _red(reduction), _ptr(loss), _ptr(lse), _ptr(workspace),
+        _nbytes(workspace), _stream(stream))
+    if raise_on_error:
+        _check(st, "flce_combine_shards")
     return st
 
 

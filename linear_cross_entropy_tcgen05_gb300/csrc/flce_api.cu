@@ -45,9 +45,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct FwdLayout {
-  size_t part_m, part_d, part_s, tgt, block_sum, block_cnt, total;
+  size_t part_m, part_d, part_s, part_idx, tgt, pred, block_sum, block_wsum, block_cnt, block_correct, total;
   int S_alloc, blocks;
 };
+
+// Header words of every workspace: [0] device error word, [16] B = g eps / V (backward),
+// [24] sum of the class weights.
+constexpr size_t kHdrErr = 0, kHdrB = 16, kHdrWtot = 24;
 
 FwdLayout fwd_layout(int64_t N, int64_t V) {
   FwdLayout L{};
@@ -59,15 +63,21 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
   L.part_m = o; o += part;
   L.part_d = o; o += part;
   L.part_s = o; o += part;
+  L.part_idx = o; o += part;
   L.tgt = o; o += align256(size_t(N) * sizeof(float));
+  L.pred = o; o += align256(size_t(N) * sizeof(int));
   L.block_sum = o; o += align256(size_t(L.blocks) * sizeof(double));
+  L.block_wsum = o; o += align256(size_t(L.blocks) * sizeof(double));
   L.block_cnt = o; o += align256(size_t(L.blocks) * sizeof(int));
+  L.block_correct = o; o += align256(size_t(L.blocks) * sizeof(int));
   L.total = o;
   return L;
 }
 
+constexpr int kColsumChunks = 64;
+
 struct BwdLayout {
-  size_t coef, band, dx_acc, total;
+  size_t coef, band, dx_acc, colsum, total;
   int64_t Vc;
 };
 
@@ -93,6 +103,7 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   L.coef = o; o += align256(size_t(N) * 16);
   L.band = o; o += align256(size_t(N) * size_t(L.Vc) * 2);
   L.dx_acc = o; o += align256(size_t(N) * size_t(D) * sizeof(float));
+  L.colsum = o; o += align256(size_t(kColsumChunks) * size_t(L.Vc) * sizeof(float));
   L.total = o;
   return L;
 }
@@ -227,147 +238,233 @@ const char* flce_status_string(flce_status st) {
 
 size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward) {
   if (!sizes_ok(N, D, V) || !sizes_in_range(N, D, V)) return 0;
-  return for_backward ? bwd_layout(N, D, V).total : fwd_layout(N, V).total;
+  const size_t f = fwd_layout(N, V).total, b = bwd_layout(N, D, V).total;
+  if (for_backward == 0) return f;
+  if (for_backward == 1) return b;
+  return f > b ? f : b;
 }
 
-flce_status flce_forward(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
-                         int32_t ignore_index, float label_smoothing, float zloss_scale, flce_reduction red,
-                         float* loss, float* lse, void* workspace, size_t ws_bytes, struct CUstream_st* stream_) {
-  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
-  if (st != FLCE_OK) return st;
-  if (!loss || !lse) return FLCE_ERR_INVALID_ARG;
-  if (!aligned(loss, 4) || !aligned(lse, 4)) return FLCE_ERR_ALIGNMENT;
-  const FwdLayout L = fwd_layout(N, V);
-  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  st = current_device(&sms);
-  if (st != FLCE_OK) return st;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* err = reinterpret_cast<int*>(ws);
+}  // extern "C"
 
-  const int64_t n_tiles = cdiv(N, gemm_tile_rows()), v_tiles = cdiv(V, kBN);
-  const int units = forward_max_units();
-  if (units <= 0) return FLCE_ERR_CUDA;
+namespace {
+
+struct Problem {
+  const void* X;
+  const void* W;
+  const int32_t* targets;
+  int64_t N, D, V;
+  int32_t ignore_index;
+  float eps, zscale;
+  flce_reduction red;
+};
+
+bool opt_ext_forward(const flce_options* o) {
+  return o && (o->softcap > 0.f || o->bias || o->class_weight || o->predicted || o->accuracy);
+}
+
+bool opt_ext_grad(const flce_options* o) { return o && (o->softcap > 0.f || o->bias || o->class_weight); }
+
+flce_status check_options(const flce_options* o, const Problem& pb, bool backward) {
+  if (!o) return FLCE_OK;
+  if (!(o->softcap >= 0.f) || std::isinf(o->softcap)) return FLCE_ERR_INVALID_ARG;
+  if ((o->bias && !aligned(o->bias, 4)) || (o->class_weight && !aligned(o->class_weight, 4)) ||
+      (o->predicted && !aligned(o->predicted, 4)) || (o->accuracy && !aligned(o->accuracy, 4)) ||
+      (o->dbias && !aligned(o->dbias, 4)) || (o->dX_f32 && !aligned(o->dX_f32, 16)))
+    return FLCE_ERR_ALIGNMENT;
+  if (o->dbias && !o->bias) return FLCE_ERR_INVALID_ARG;
+  const bool shard = o->v_total != 0 && o->v_total != pb.V;
+  if (shard) {
+    if (!backward) return FLCE_ERR_INVALID_ARG;  // forward shards go through flce_shard_stats
+    if (o->v_total < pb.V || o->v_offset < 0 || o->v_offset + pb.V > o->v_total) return FLCE_ERR_INVALID_ARG;
+    if (o->v_total >= (int64_t(1) << 30)) return FLCE_ERR_TOO_LARGE;
+    if (o->softcap > 0.f || o->bias || o->class_weight || o->dbias) return FLCE_ERR_INVALID_ARG;
+  } else if (o->v_offset != 0) {
+    return FLCE_ERR_INVALID_ARG;
+  }
+  return FLCE_OK;
+}
+
+// Forward GEMM + finalize. mode FIN_LOSS (loss, lse, options) or FIN_SHARD_STATS.
+flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, int64_t v_offset, float* loss,
+                        float* lse, float* stats, uint8_t* ws, bool clear_header, int units, cudaStream_t stream) {
+  const FwdLayout L = fwd_layout(pb.N, pb.V);
+  int* err = reinterpret_cast<int*>(ws + kHdrErr);
+  float* wtot = reinterpret_cast<float*>(ws + kHdrWtot);
+  const int64_t n_tiles = cdiv(pb.N, gemm_tile_rows()), v_tiles = cdiv(pb.V, kBN);
   int gN = 1, S = 1;
   pick_forward_grid(units, n_tiles, v_tiles, L.S_alloc, &gN, &S);
 
   CUtensorMap tmX, tmW;
-  if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) ||
-      !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, 64))
+  if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
+                 64, kBM) ||
+      !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
+                 64, 64))
     return FLCE_ERR_CUDA;
 
-  FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  const float* cw = opt ? opt->class_weight : nullptr;
+  if (cw) FLCE_CUDA_CHECK(launch_sum(cw, int(pb.V), wtot, stream));
+  const bool ext = mode == FIN_LOSS && opt_ext_forward(opt);
+  const bool want_idx = ext && (opt->predicted || opt->accuracy);
+
   FwdParams p{};
-  p.targets = targets;
-  p.N = int(N);
-  p.V = int(V);
+  p.targets = pb.targets;
+  p.N = int(pb.N);
+  p.V = int(pb.V);
   p.n_tiles = int(n_tiles);
   p.v_tiles = int(v_tiles);
   p.gN = gN;
   p.S = S;
-  p.num_kb = int(cdiv(D, kBK));
-  p.want_sum_z = label_smoothing != 0.f;
+  p.num_kb = int(cdiv(pb.D, kBK));
+  p.want_sum_z = (mode == FIN_SHARD_STATS) || pb.eps != 0.f;
+  p.ignore_index = pb.ignore_index;
+  p.y_offset = int(v_offset);
   p.part_m = reinterpret_cast<float*>(ws + L.part_m);
   p.part_d = reinterpret_cast<float*>(ws + L.part_d);
   p.part_s = reinterpret_cast<float*>(ws + L.part_s);
   p.tgt = reinterpret_cast<float*>(ws + L.tgt);
   p.err = err;
-  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, stream));
+  if (ext) {
+    p.bias = opt->bias;
+    p.cw = cw;
+    p.softcap = opt->softcap;
+    p.part_idx = want_idx ? reinterpret_cast<int*>(ws + L.part_idx) : nullptr;
+  }
+  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, ext, stream));
 
   FinalizeParams f{};
+  f.mode = mode;
   f.part_m = p.part_m;
   f.part_d = p.part_d;
   f.part_s = p.part_s;
   f.tgt = p.tgt;
-  f.targets = targets;
-  f.N = int(N);
-  f.V = int(V);
+  f.part_idx = p.part_idx;
+  f.targets = pb.targets;
+  f.N = int(pb.N);
+  f.V = int(pb.V);
   f.S = S;
-  f.ignore_index = ignore_index;
-  f.eps = label_smoothing;
-  f.zscale = zloss_scale;
-  f.reduction = int(red);
+  f.V_local = int(pb.V);
+  f.v_offset = int(v_offset);
+  f.ignore_index = pb.ignore_index;
+  f.eps = pb.eps;
+  f.zscale = pb.zscale;
+  f.reduction = int(pb.red);
+  f.cw = ext ? cw : nullptr;
+  f.wtot = wtot;
   f.lse = lse;
   f.loss = loss;
+  f.stats_out = stats;
+  // The argmax decision is made per row in the finalize; without a caller array it
+  // lands in scratch (accuracy only).
+  f.predicted = want_idx ? (opt->predicted ? opt->predicted : reinterpret_cast<int*>(ws + L.pred)) : nullptr;
+  f.accuracy = want_idx ? opt->accuracy : nullptr;
   f.block_sum = reinterpret_cast<double*>(ws + L.block_sum);
+  f.block_wsum = reinterpret_cast<double*>(ws + L.block_wsum);
   f.block_cnt = reinterpret_cast<int*>(ws + L.block_cnt);
+  f.block_correct = reinterpret_cast<int*>(ws + L.block_correct);
   f.err = err;
   FLCE_CUDA_CHECK(launch_finalize(f, L.blocks, stream));
   return FLCE_OK;
 }
 
-flce_status flce_backward(const void* X, const void* W, const int32_t* targets, const float* lse, int64_t N,
-                          int64_t D, int64_t V, int32_t ignore_index, float label_smoothing, float zloss_scale,
-                          flce_reduction red, const float* grad_out, void* dX, float* dW, void* workspace,
-                          size_t ws_bytes, struct CUstream_st* stream_) {
-  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
-  if (st != FLCE_OK) return st;
-  if (!lse || !grad_out || !dX || !dW) return FLCE_ERR_INVALID_ARG;
-  if (red == FLCE_REDUCTION_NONE) return FLCE_ERR_REDUCTION_NONE_GRAD;
-  if (!aligned(lse, 4) || !aligned(grad_out, 4) || !aligned(dX, 16) || !aligned(dW, 16)) return FLCE_ERR_ALIGNMENT;
-  const BwdLayout L = bwd_layout(N, D, V);
-  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  st = current_device(&sms);
-  if (st != FLCE_OK) return st;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* err = reinterpret_cast<int*>(ws);
-  float* cval = reinterpret_cast<float*>(ws + 16);
+flce_status run_backward(const Problem& pb, const flce_options* opt, const float* lse, const float* grad_out,
+                         void* dX, float* dW, uint8_t* ws, bool clear_header, int sms, cudaStream_t stream) {
+  const BwdLayout L = bwd_layout(pb.N, pb.D, pb.V);
+  int* err = reinterpret_cast<int*>(ws + kHdrErr);
+  float* bval = reinterpret_cast<float*>(ws + kHdrB);
+  float* wtot = reinterpret_cast<float*>(ws + kHdrWtot);
   float4* coef = reinterpret_cast<float4*>(ws + L.coef);
   void* band = ws + L.band;
-  float* dx_acc = reinterpret_cast<float*>(ws + L.dx_acc);
+  float* dx_f32 = (opt && opt->dX_f32) ? opt->dX_f32 : reinterpret_cast<float*>(ws + L.dx_acc);
   const int64_t Vc = L.Vc;
+  const bool shard = opt && opt->v_total != 0 && opt->v_total != pb.V;
+  const int64_t V_total = shard ? opt->v_total : pb.V;
+  const int64_t v_offset = shard ? opt->v_offset : 0;
+  const float* cw = opt ? opt->class_weight : nullptr;
+  const bool ext = opt_ext_grad(opt);
 
   CUtensorMap tmXk, tmXmn, tmWmn, tmWk, tmG, tmGmn, tmDW, tmDX;
   const bool enc =
-      encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, kBM) &&
-      encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, uint64_t(D), uint64_t(N), uint64_t(D), 64, 64) &&
-      encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64, 64) &&
-      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, uint64_t(V), uint64_t(D), uint64_t(V), 64,
+      encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64,
+                kBM) &&
+      encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64,
+                64) &&
+      encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64,
+                64) &&
+      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64,
                 uint32_t(gemm_b_rows_per_cta())) &&
-      encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, kBM) &&
-      encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(N), uint64_t(Vc), 64, 64) &&
-      encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(V), uint64_t(D), uint64_t(V), 32, kBM) &&
-      encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_acc, uint64_t(D), uint64_t(N), uint64_t(D), 32, kBM);
+      encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(pb.N), uint64_t(Vc), 64,
+                kBM) &&
+      encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(pb.N), uint64_t(Vc), 64,
+                64) &&
+      encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 32,
+                kBM) &&
+      encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_f32, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
+                32, kBM);
   if (!enc) return FLCE_ERR_CUDA;
 
-  FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
+  if (cw) FLCE_CUDA_CHECK(launch_sum(cw, int(pb.V), wtot, stream));
   PrepParams pp{};
-  pp.targets = targets;
+  pp.targets = pb.targets;
   pp.lse = lse;
   pp.grad_out = grad_out;
-  pp.N = int(N);
-  pp.V = int(V);
-  pp.ignore_index = ignore_index;
-  pp.eps = label_smoothing;
-  pp.zscale = zloss_scale;
-  pp.reduction = int(red);
+  pp.N = int(pb.N);
+  pp.V = int(V_total);
+  pp.y_offset = int(v_offset);
+  pp.ignore_index = pb.ignore_index;
+  pp.eps = pb.eps;
+  pp.zscale = pb.zscale;
+  pp.reduction = int(pb.red);
+  pp.cw = cw;
+  pp.wtot = wtot;
   pp.coef = coef;
-  pp.cval = cval;
+  pp.bval = bval;
   pp.err = err;
   FLCE_CUDA_CHECK(launch_prep(pp, stream));
 
-  const int64_t n_tiles = cdiv(N, gemm_tile_rows());
-  const int64_t d_tiles_m = cdiv(D, gemm_tile_rows());  // dW rows
-  const int64_t d_tiles_n = cdiv(D, kBN);               // dX columns
-  for (int64_t v0 = 0, band_i = 0; v0 < V; v0 += Vc, ++band_i) {
-    const int64_t vc = (V - v0 < Vc) ? V - v0 : Vc;
+  const int64_t n_tiles = cdiv(pb.N, gemm_tile_rows());
+  const int64_t d_tiles_m = cdiv(pb.D, gemm_tile_rows());  // dW rows
+  const int64_t d_tiles_n = cdiv(pb.D, kBN);               // dX columns
+  for (int64_t v0 = 0, band_i = 0; v0 < pb.V; v0 += Vc, ++band_i) {
+    const int64_t vc = (pb.V - v0 < Vc) ? pb.V - v0 : Vc;
     const int64_t vt = cdiv(vc, kBN);
 
     WalkParams wg{};
     wg.total_tiles = int(n_tiles * vt);
     wg.tiles_minor = int(vt);
-    wg.num_kb = int(cdiv(D, kBK));
+    wg.num_kb = int(cdiv(pb.D, kBK));
     wg.b_row_off = int(v0);
-    GradEpiParams ge{coef, cval, int(N), int(V), int(v0), err};
-    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, stream));
+    GradEpiParams ge{};
+    ge.coef = coef;
+    ge.bval = bval;
+    ge.N = int(pb.N);
+    ge.V = int(pb.V);
+    ge.chunk_v0 = int(v0);
+    ge.err = err;
+    if (ext) {
+      ge.bias = opt->bias;
+      ge.cw = cw;
+      ge.softcap = opt->softcap;
+    }
+    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, ext, stream));
+
+    if (opt && opt->dbias) {
+      ColsumParams cp{};
+      cp.band = static_cast<const uint16_t*>(band);
+      cp.N = int(pb.N);
+      cp.ld = int(Vc);
+      cp.cols = int(vc);
+      cp.row_chunks = kColsumChunks;
+      cp.partial = reinterpret_cast<float*>(ws + L.colsum);
+      cp.out = opt->dbias + v0;
+      FLCE_CUDA_CHECK(launch_colsum(cp, stream));
+    }
 
     WalkParams ww{};
     ww.total_tiles = int(vt * d_tiles_m);
     ww.tiles_minor = int(d_tiles_m);
-    ww.num_kb = int(cdiv(N, kBK));
+    ww.num_kb = int(cdiv(pb.N, kBK));
     StoreEpiParams sw{0, int(v0), err};
     FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
 
@@ -379,7 +476,159 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
     StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
     FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx, stream));
   }
-  FLCE_CUDA_CHECK(launch_cast_bf16(dx_acc, dX, size_t(N) * size_t(D), sms, stream));
+  if (!(opt && opt->dX_f32))
+    FLCE_CUDA_CHECK(launch_cast_bf16(dx_f32, dX, size_t(pb.N) * size_t(pb.D), sms, stream));
+  return FLCE_OK;
+}
+
+flce_status check_forward_outputs(const float* loss, const float* lse) {
+  if (!loss || !lse) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(loss, 4) || !aligned(lse, 4)) return FLCE_ERR_ALIGNMENT;
+  return FLCE_OK;
+}
+
+flce_status check_backward_outputs(const Problem& pb, const flce_options* opt, const float* lse,
+                                   const float* grad_out, const void* dX, const float* dW) {
+  const bool f32 = opt && opt->dX_f32;
+  if (!lse || !grad_out || (!dX && !f32) || !dW) return FLCE_ERR_INVALID_ARG;
+  if (pb.red == FLCE_REDUCTION_NONE) return FLCE_ERR_REDUCTION_NONE_GRAD;
+  if (!aligned(lse, 4) || !aligned(grad_out, 4) || (!f32 && !aligned(dX, 16)) || !aligned(dW, 16))
+    return FLCE_ERR_ALIGNMENT;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
+                            int32_t ignore_index, float label_smoothing, float zloss_scale, flce_reduction red,
+                            const flce_options* opt, float* loss, float* lse, void* workspace, size_t ws_bytes,
+                            struct CUstream_st* stream) {
+  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
+  if (st != FLCE_OK) return st;
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
+  if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
+  if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  const int units = forward_max_units();
+  if (units <= 0) return FLCE_ERR_CUDA;
+  return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), true, units,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_forward(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
+                         int32_t ignore_index, float label_smoothing, float zloss_scale, flce_reduction red,
+                         float* loss, float* lse, void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+  return flce_forward_ex(X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, nullptr, loss,
+                         lse, workspace, ws_bytes, stream);
+}
+
+flce_status flce_backward_ex(const void* X, const void* W, const int32_t* targets, const float* lse, int64_t N,
+                             int64_t D, int64_t V, int32_t ignore_index, float label_smoothing, float zloss_scale,
+                             flce_reduction red, const flce_options* opt, const float* grad_out, void* dX, float* dW,
+                             void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
+  if (st != FLCE_OK) return st;
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
+  if ((st = check_options(opt, pb, true)) != FLCE_OK) return st;
+  if (ws_bytes < bwd_layout(N, D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  return run_backward(pb, opt, lse, grad_out, dX, dW, static_cast<uint8_t*>(workspace), true, sms,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_backward(const void* X, const void* W, const int32_t* targets, const float* lse, int64_t N,
+                          int64_t D, int64_t V, int32_t ignore_index, float label_smoothing, float zloss_scale,
+                          flce_reduction red, const float* grad_out, void* dX, float* dW, void* workspace,
+                          size_t ws_bytes, struct CUstream_st* stream) {
+  return flce_backward_ex(X, W, targets, lse, N, D, V, ignore_index, label_smoothing, zloss_scale, red, nullptr,
+                          grad_out, dX, dW, workspace, ws_bytes, stream);
+}
+
+flce_status flce_forward_backward(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D,
+                                  int64_t V, int32_t ignore_index, float label_smoothing, float zloss_scale,
+                                  flce_reduction red, const flce_options* opt, const float* grad_out, float* loss,
+                                  float* lse, void* dX, float* dW, void* workspace, size_t ws_bytes,
+                                  struct CUstream_st* stream) {
+  flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
+  if (st != FLCE_OK) return st;
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
+  if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
+  if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
+  if (ws_bytes < flce_workspace_size(N, D, V, 2)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  const int units = forward_max_units();
+  if (units <= 0) return FLCE_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, true, units, s)) != FLCE_OK) return st;
+  return run_backward(pb, opt, lse, grad_out, dX, dW, ws, false, sms, s);
+}
+
+flce_status flce_shard_stats(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
+                             int64_t v_offset, int32_t ignore_index, float* stats, void* workspace, size_t ws_bytes,
+                             struct CUstream_st* stream) {
+  flce_status st = check_common(X, W, targets, N, D, V, 0.f, 0.f, 0, workspace);
+  if (st != FLCE_OK) return st;
+  if (!stats) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(stats, 4)) return FLCE_ERR_ALIGNMENT;
+  if (v_offset < 0) return FLCE_ERR_INVALID_ARG;
+  if (v_offset + V >= (int64_t(1) << 30)) return FLCE_ERR_TOO_LARGE;
+  if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  const int units = forward_max_units();
+  if (units <= 0) return FLCE_ERR_CUDA;
+  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM};
+  return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
+                     static_cast<uint8_t*>(workspace), true, units, reinterpret_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* targets, int64_t N, int64_t v_total,
+                                int32_t ignore_index, float label_smoothing, float zloss_scale, flce_reduction red,
+                                float* loss, float* lse, void* workspace, size_t ws_bytes,
+                                struct CUstream_st* stream) {
+  if (!stats || !targets || !workspace || K < 1 || N < 1 || v_total < 1) return FLCE_ERR_INVALID_ARG;
+  if (!(label_smoothing >= 0.f && label_smoothing < 1.f) || !(zloss_scale >= 0.f) || std::isinf(zloss_scale) ||
+      int(red) < 0 || int(red) > 2)
+    return FLCE_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 30) || v_total >= (int64_t(1) << 30) || K > 4096) return FLCE_ERR_TOO_LARGE;
+  flce_status st = check_forward_outputs(loss, lse);
+  if (st != FLCE_OK) return st;
+  if (!aligned(stats, 4) || !aligned(targets, 4) || !aligned(workspace, 16)) return FLCE_ERR_ALIGNMENT;
+  const FwdLayout L = fwd_layout(N, 8);
+  if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, s));
+  FinalizeParams f{};
+  f.mode = FIN_COMBINE;
+  f.stats = stats;
+  f.targets = targets;
+  f.N = int(N);
+  f.V = int(v_total);
+  f.S = K;
+  f.ignore_index = ignore_index;
+  f.eps = label_smoothing;
+  f.zscale = zloss_scale;
+  f.reduction = int(red);
+  f.lse = lse;
+  f.loss = loss;
+  f.block_sum = reinterpret_cast<double*>(ws + L.block_sum);
+  f.block_wsum = reinterpret_cast<double*>(ws + L.block_wsum);
+  f.block_cnt = reinterpret_cast<int*>(ws + L.block_cnt);
+  f.block_correct = reinterpret_cast<int*>(ws + L.block_correct);
+  f.err = reinterpret_cast<int*>(ws + kHdrErr);
+  FLCE_CUDA_CHECK(launch_finalize(f, L.blocks, s));
   return FLCE_OK;
 }
 

@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "flce_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -464,7 +466,67 @@ __device__ __forceinline__ void online_update(RowStats& st, const uint32_t (&r)[
   }
 }
 
-template <int CG, int STAGES>
+// Extended variant: logits u = softcap(z + bias_j), sum of w_j u_j, first argmax column.
+struct RowStatsExt {
+  float m, d, sz, zy;
+  bool cap;
+  int idx;
+};
+
+template <bool kMasked>
+__device__ __forceinline__ void online_update_ext(RowStatsExt& st, const uint32_t (&r)[32], int col0, int V, int y,
+                                                  bool want_sum, const FwdParams& p) {
+  float v[32];
+  float w[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool in = !kMasked || col0 + j < V;
+    float z = __uint_as_float(r[j]);
+    if (p.bias != nullptr && in) z += __ldg(p.bias + col0 + j);
+    if (p.softcap > 0.f) z = p.softcap * tanhf(z / p.softcap);
+    v[j] = in ? z : -CUDART_INF_F;
+    w[j] = (p.cw != nullptr && in) ? __ldg(p.cw + col0 + j) : (in ? 1.f : 0.f);
+  }
+  const int rel = y - col0;
+  if (static_cast<unsigned>(rel) < 32u) {
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) z = (j == rel) ? v[j] : z;
+    st.zy = z;
+    st.cap = true;
+  }
+  float cm = v[0];
+#pragma unroll
+  for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
+  if (cm > st.m) {  // strictly greater: an earlier column keeps ties
+    int first = 31;
+#pragma unroll
+    for (int j = 31; j >= 0; --j) first = (v[j] == cm) ? j : first;
+    st.idx = col0 + first;
+  }
+  const float nm = fmaxf(st.m, cm);
+  const float scale = exp2f((st.m - nm) * kLog2e);
+  const float nml = nm * kLog2e;
+  float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    e0 += exp2f(fmaf(v[j], kLog2e, -nml));
+    e1 += exp2f(fmaf(v[j + 1], kLog2e, -nml));
+  }
+  st.d = st.d * scale + (e0 + e1);
+  st.m = nm;
+  if (want_sum) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      s0 += (w[j] != 0.f) ? w[j] * v[j] : 0.f;
+      s1 += (w[j + 1] != 0.f) ? w[j + 1] * v[j + 1] : 0.f;
+    }
+    st.sz += s0 + s1;
+  }
+}
+
+template <int CG, int STAGES, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_forward_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const FwdParams p) {
@@ -495,15 +557,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
-    RowStats st{-CUDART_INF_F, 0.f, 0.f, 0.f, false};
+    using Stats = typename std::conditional<EXT, RowStatsExt, RowStats>::type;
+    Stats st{};
     int row = 0, y = -1;
     const bool want_sum = p.want_sum_z != 0;
     while (sched.next(t)) {
       if (!epi_acquire(s, acc, acc_phase, epi_tid, w)) break;
       if (t.flags & TILE_FIRST) {
         row = t.a_row + r;
-        y = (row < p.N) ? __ldg(p.targets + row) : -1;
-        st = RowStats{-CUDART_INF_F, 0.f, 0.f, 0.f, false};
+        y = -1;
+        if (row < p.N) {
+          const int yt = __ldg(p.targets + row);
+          y = (yt == p.ignore_index) ? -1 : yt - p.y_offset;
+        }
+        st = Stats{};
+        st.m = -CUDART_INF_F;
       }
       const uint32_t taddr = lane_addr + uint32_t(acc * kBN);
       const bool tail_tile = t.b_row + kBN > p.V;
@@ -515,12 +583,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_ld();
         if (c + 64 == kBN) epi_release<CG>(s, acc);
         const int col0 = t.b_row + c;
-        if (!tail_tile) {
-          online_update<false>(st, r0, col0, p.V, y, want_sum);
-          online_update<false>(st, r1, col0 + 32, p.V, y, want_sum);
+        if constexpr (EXT) {
+          if (!tail_tile) {
+            online_update_ext<false>(st, r0, col0, p.V, y, want_sum, p);
+            online_update_ext<false>(st, r1, col0 + 32, p.V, y, want_sum, p);
+          } else {
+            if (col0 < p.V) online_update_ext<true>(st, r0, col0, p.V, y, want_sum, p);
+            if (col0 + 32 < p.V) online_update_ext<true>(st, r1, col0 + 32, p.V, y, want_sum, p);
+          }
         } else {
-          if (col0 < p.V) online_update<true>(st, r0, col0, p.V, y, want_sum);
-          if (col0 + 32 < p.V) online_update<true>(st, r1, col0 + 32, p.V, y, want_sum);
+          if (!tail_tile) {
+            online_update<false>(st, r0, col0, p.V, y, want_sum);
+            online_update<false>(st, r1, col0 + 32, p.V, y, want_sum);
+          } else {
+            if (col0 < p.V) online_update<true>(st, r0, col0, p.V, y, want_sum);
+            if (col0 + 32 < p.V) online_update<true>(st, r1, col0 + 32, p.V, y, want_sum);
+          }
         }
       }
       if ((t.flags & TILE_LAST) && row < p.N) {
@@ -529,6 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.part_d[o] = st.d;
         p.part_s[o] = st.sz;
         if (st.cap) p.tgt[row] = st.zy;
+        if constexpr (EXT) {
+          if (p.part_idx != nullptr) p.part_idx[o] = st.idx;
+        }
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -569,7 +650,7 @@ __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32
   }
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI>
+template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_walk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const WalkParams wp, const GradEpiParams gp,
@@ -608,12 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epi_acquire(s, acc, acc_phase, epi_tid, w)) break;
       const uint32_t taddr = lane_addr + uint32_t(acc * kBN);
       if (EPI == 0) {
-        // G = a * exp2(z*log2e - lse*log2e) - b - [col == y] c, zero outside the vocabulary.
+        // G = A exp2(u log2e - lse log2e) - B w_j - [col == y] C (times 1 - (u/c)^2 with a
+        // softcap), zero outside the vocabulary and on ignored rows.
         const int row = t.a_row + r;
-        float4 cf = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+        float4 cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
         if (row < gp.N) cf = __ldg(gp.coef + row);
-        const float cval = __ldg(gp.cval);
         const int y = __float_as_int(cf.w);
+        const float brow = (y == kIgnoredRow) ? 0.f : __ldg(gp.bval);
 #pragma unroll 1
         for (int c = 0; c < kBN; c += 64) {
           uint32_t r0[32], r1[32];
@@ -626,16 +708,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t* packed = reinterpret_cast<uint32_t*>(chunks);
 #pragma unroll
           for (int j = 0; j < 64; j += 2) {
-            const float z0 = __uint_as_float(j < 32 ? r0[j] : r1[j - 32]);
-            const float z1 = __uint_as_float(j + 1 < 32 ? r0[j + 1] : r1[j + 1 - 32]);
-            float g0 = cf.x * exp2f(fmaf(z0, kLog2e, cf.y)) - cf.z;
-            float g1 = cf.x * exp2f(fmaf(z1, kLog2e, cf.y)) - cf.z;
-            if (col0 + j == y) g0 -= cval;
-            if (col0 + j + 1 == y) g1 -= cval;
-            if (col0 + j >= gp.V) g0 = 0.f;
-            if (col0 + j + 1 >= gp.V) g1 = 0.f;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
-            packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+            float gg[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int jj = j + h;
+              const int col = col0 + jj;
+              float u = __uint_as_float(jj < 32 ? r0[jj] : r1[jj - 32]);
+              float g;
+              if constexpr (EXT) {
+                const bool in = col < gp.V;
+                if (gp.bias != nullptr && in) u += __ldg(gp.bias + col);
+                float dcap = 1.f;
+                if (gp.softcap > 0.f) {
+                  u = gp.softcap * tanhf(u / gp.softcap);
+                  const float q = u / gp.softcap;
+                  dcap = 1.f - q * q;
+                }
+                const float wj = (gp.cw != nullptr && in) ? __ldg(gp.cw + col) : 1.f;
+                g = cf.x * exp2f(fmaf(u, kLog2e, cf.y)) - brow * wj;
+                if (col == y) g -= cf.z;
+                g *= dcap;
+              } else {
+                g = cf.x * exp2f(fmaf(u, kLog2e, cf.y)) - brow;
+                if (col == y) g -= cf.z;
+              }
+              gg[h] = (col >= gp.V) ? 0.f : g;
+            }
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(gg[0], gg[1]);
+            packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           epi_store_box(
               s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
@@ -715,10 +815,12 @@ int max_clusters(Kern kernel, size_t smem, int slot) {
   return n;
 }
 
-auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kFwdStages>; }
-auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, true, WALK_GRAD, 0>; }
-auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, true, true, WALK_DW, 1>; }
-auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, false, WALK_DX, 1>; }
+template <bool EXT>
+auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kFwdStages, EXT>; }
+template <bool EXT>
+auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, true, WALK_GRAD, 0, EXT>; }
+auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, true, true, WALK_DW, 1, false>; }
+auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, false, WALK_DX, 1, false>; }
 
 constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
 constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
@@ -744,11 +846,12 @@ int gemm_tile_rows() { return kBM * kCG; }
 
 int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
 
-int forward_max_units() { return max_clusters(fwd_kernel(), kFwdSmem, 0); }
+// Both forward instantiations share the launch shape (same shared memory and threads).
+int forward_max_units() { return max_clusters(fwd_kernel<false>(), kFwdSmem, 0); }
 
-cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p,
+cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
                                 cudaStream_t stream) {
-  auto kern = fwd_kernel();
+  auto kern = ext ? fwd_kernel<true>() : fwd_kernel<false>();
   cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -757,20 +860,23 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 }
 
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, cudaStream_t stream) {
+                             const WalkParams& w, const GradEpiParams& e, bool ext, cudaStream_t stream) {
   StoreEpiParams unused{0, 0, e.err};
-  return launch_walk(grad_kernel(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  if (ext) return launch_walk(grad_kernel<true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  return launch_walk(grad_kernel<false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
-  GradEpiParams unused{nullptr, nullptr, 0, 0, 0, e.err};
+  GradEpiParams unused{};
+  unused.err = e.err;
   return launch_walk(dw_kernel(), tmA, tmB, tmC, w, unused, e, 2, stream);
 }
 
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
-  GradEpiParams unused{nullptr, nullptr, 0, 0, 0, e.err};
+  GradEpiParams unused{};
+  unused.err = e.err;
   return launch_walk(dx_kernel(), tmA, tmB, tmC, w, unused, e, 3, stream);
 }
 

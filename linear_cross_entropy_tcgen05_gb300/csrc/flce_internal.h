@@ -42,6 +42,9 @@ struct WalkParams {
   int b_row_off;     // added to the B operand's row/column coordinate
 };
 
+// Sentinel target of an ignored row in the per-row gradient coefficients.
+constexpr int kIgnoredRow = int(0x80000000);
+
 struct FwdParams {
   const int32_t* targets;
   int N, V;
@@ -49,19 +52,30 @@ struct FwdParams {
   int gN, S;       // grid = gN row tiles x S vocabulary ranges (CTA pairs)
   int num_kb;      // K blocks over D
   int want_sum_z;  // label smoothing needs sum_j z_ij
+  int ignore_index;
+  int y_offset;    // vocabulary shard: global index of W's first column
   float* part_m;   // [S][N] running max
   float* part_d;   // [S][N] sum of exp(z - max)
-  float* part_s;   // [S][N] sum of z
+  float* part_s;   // [S][N] sum of z (sum of w_j u_j with class weights)
   float* tgt;      // [N] target logit
   int* err;
+  // extended epilogue only
+  const float* bias;  // [V] or null
+  const float* cw;    // [V] class weights or null
+  float softcap;      // 0: off
+  int* part_idx;      // [S][N] first column of the range maximum, or null
 };
 
 struct GradEpiParams {
-  const float4* coef;  // per row {a, -lse*log2e, b, bits(target or -1)}
-  const float* cval;   // device scalar: g (1 - eps), subtracted at the target column
+  const float4* coef;  // per row {A, -lse*log2e, C, target column in W (or kIgnoredRow)}
+  const float* bval;   // device scalar B = g eps / V_total: G -= B w_j on valid rows
   int N, V;
   int chunk_v0;        // first vocabulary column of the current band
   int* err;
+  // extended epilogue only
+  const float* bias;  // [V] or null
+  const float* cw;    // [V] or null
+  float softcap;      // 0: off
 };
 
 struct StoreEpiParams {
@@ -70,20 +84,34 @@ struct StoreEpiParams {
   int* err;
 };
 
+enum FinalizeMode : int { FIN_LOSS = 0, FIN_SHARD_STATS = 1, FIN_COMBINE = 2 };
+
 struct FinalizeParams {
-  const float* part_m;
+  int mode;
+  const float* part_m;  // FIN_LOSS / FIN_SHARD_STATS: [S][N] partials of the forward GEMM
   const float* part_d;
   const float* part_s;
   const float* tgt;
+  const int* part_idx;  // [S][N] or null (argmax)
+  const float* stats;   // FIN_COMBINE: [S][4][N] shard statistics (S = shard count)
   const int32_t* targets;
-  int N, V, S;
+  int N, V, S;          // V: the full vocabulary (v_total)
+  int V_local;          // FIN_SHARD_STATS: columns of this shard
+  int v_offset;         // FIN_SHARD_STATS: global index of the shard's first column
   int ignore_index;
   float eps, zscale;
   int reduction;        // 0 mean, 1 sum, 2 none
+  const float* cw;      // [V] class weights or null
+  const float* wtot;    // device scalar sum_j w_j (with cw)
   float* lse;
   float* loss;          // [1] or [N]
-  double* block_sum;    // [blocks]
-  int* block_cnt;       // [blocks]
+  float* stats_out;     // FIN_SHARD_STATS: [4][N]
+  int* predicted;       // [N] or null
+  float* accuracy;      // [1] or null
+  double* block_sum;    // [blocks] loss partial sums
+  double* block_wsum;   // [blocks] mean denominators (valid rows or their weights)
+  int* block_cnt;       // [blocks] valid rows
+  int* block_correct;   // [blocks] argmax hits
   int* err;
 };
 
@@ -91,13 +119,25 @@ struct PrepParams {
   const int32_t* targets;
   const float* lse;
   const float* grad_out;
-  int N, V;
+  int N;
+  int V;                // full vocabulary (v_total)
+  int y_offset;         // vocabulary shard: global index of W's first column
   int ignore_index;
   float eps, zscale;
   int reduction;
+  const float* cw;      // [V] class weights or null
+  const float* wtot;    // device scalar sum_j w_j (with cw)
   float4* coef;
-  float* cval;
+  float* bval;
   int* err;
+};
+
+struct ColsumParams {
+  const uint16_t* band;  // bf16 [N][ld]
+  int N, ld, cols;
+  int row_chunks;
+  float* partial;        // [row_chunks][cols]
+  float* out;            // [cols]
 };
 
 // Rows of one GEMM output tile (a CTA pair: 2 x 128).
@@ -107,13 +147,18 @@ int gemm_b_rows_per_cta();
 // CTA pairs of the forward GEMM that can be resident at once on the current device.
 int forward_max_units();
 
-cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p,
+// ext: the extended epilogue (bias, softcap, class weights, argmax); else the plain one.
+cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
                                 cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream);
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+// out[0] = sum of v[0..n) in a fixed order (one block).
+cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream);
+// Column sums of a bf16 band, fixed order (two kernels).
+cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream);
 // The walk GEMMs size their own grids: min(tiles, resident CTA pairs) clusters of 2.
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, cudaStream_t stream);
+                             const WalkParams& w, const GradEpiParams& e, bool ext, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

@@ -17,138 +17,243 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------------
 // ---------------------------------------------------------------------------------
 
-// Combine the S partial statistics of each row into lse, form the row loss and
-// reduce it deterministically (per-block fp64 partial sums, then one block).
+// Combine each row's partial statistics into lse and the row loss (FIN_LOSS), into one
+// vocabulary shard's statistics (FIN_SHARD_STATS), or combine K shards' statistics
+// (FIN_COMBINE); then reduce the loss deterministically (per-block fp64 partial sums,
+// then one block).
 __global__ void __launch_bounds__(kFinalizeThreads)
     flce_finalize_rows_kernel(const FinalizeParams p) {
   const int row = int(blockIdx.x) * kFinalizeThreads + int(threadIdx.x);
-  double contrib = 0.0;
-  int valid = 0;
+  double contrib = 0.0, den = 0.0;
+  int valid = 0, correct = 0;
   if (row < p.N) {
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.part_m[size_t(s) * p.N + row]);
-    float d = 0.f, sz = 0.f;
-    for (int s = 0; s < p.S; ++s) {
-      const size_t o = size_t(s) * p.N + row;
-      d += p.part_d[o] * exp2f((p.part_m[o] - M) * kLog2e);
-      sz += p.part_s[o];
+    float M = -CUDART_INF_F, d = 0.f, sz = 0.f, zy = 0.f;
+    int owners = 0, best_idx = 0;
+    if (p.mode == FIN_COMBINE) {
+      for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.stats[(size_t(s) * 4 + 0) * p.N + row]);
+      for (int s = 0; s < p.S; ++s) {
+        const float* st = p.stats + size_t(s) * 4 * p.N;
+        d += exp2f((st[row] - M) * kLog2e);
+        sz += st[size_t(p.N) + row];
+        zy += st[2 * size_t(p.N) + row];
+        owners += st[3 * size_t(p.N) + row] != 0.f ? 1 : 0;
+      }
+    } else {
+      float best = -CUDART_INF_F;
+      for (int s = 0; s < p.S; ++s) {
+        const float m = p.part_m[size_t(s) * p.N + row];
+        M = fmaxf(M, m);
+        if (p.part_idx != nullptr) {
+          const int idx = p.part_idx[size_t(s) * p.N + row];
+          if (m > best || (m == best && idx < best_idx)) {
+            best = m;
+            best_idx = idx;
+          }
+        }
+      }
+      for (int s = 0; s < p.S; ++s) {
+        const size_t o = size_t(s) * p.N + row;
+        d += p.part_d[o] * exp2f((p.part_m[o] - M) * kLog2e);
+        sz += p.part_s[o];
+      }
+      zy = p.tgt[row];
     }
     const float lse = M + logf(d);
-    p.lse[row] = lse;
     const int y = p.targets[row];
+    if (p.mode == FIN_SHARD_STATS) {
+      const int rel = y - p.v_offset;
+      const bool own = y != p.ignore_index && rel >= 0 && rel < p.V_local;
+      p.stats_out[row] = lse;
+      p.stats_out[size_t(p.N) + row] = sz;
+      p.stats_out[2 * size_t(p.N) + row] = own ? zy : 0.f;
+      p.stats_out[3 * size_t(p.N) + row] = own ? 1.f : 0.f;
+      return;
+    }
+    p.lse[row] = lse;
+    if (p.predicted != nullptr) p.predicted[row] = best_idx;
     float ell = 0.f;
     if (y != p.ignore_index) {
       valid = 1;
-      if (y < 0 || y >= p.V) {
+      const bool bad = y < 0 || y >= p.V || (p.mode == FIN_COMBINE && owners != 1);
+      if (bad) {
         atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
         ell = CUDART_NAN_F;
+        den = 1.0;
       } else {
-        const float zy = p.tgt[row];
-        ell = (1.f - p.eps) * (lse - zy) + p.zscale * lse * lse;
-        if (p.eps != 0.f) ell += p.eps * (lse - sz / float(p.V));
+        const float wy = p.cw != nullptr ? p.cw[y] : 1.f;
+        const float wtot = p.cw != nullptr ? *p.wtot : float(p.V);
+        ell = (1.f - p.eps) * wy * (lse - zy) + p.zscale * lse * lse;
+        if (p.eps != 0.f) ell += p.eps / float(p.V) * (wtot * lse - sz);
+        den = double(wy);
+        correct = (p.predicted != nullptr && best_idx == y) ? 1 : 0;
       }
     }
     if (p.reduction == 2) p.loss[row] = ell;
     contrib = double(ell);
   }
-  if (p.reduction == 2) return;
+  if (p.mode == FIN_SHARD_STATS) return;
   // fixed-order block reduction
   __shared__ double ssum[kFinalizeThreads];
+  __shared__ double sden[kFinalizeThreads];
   __shared__ int scnt[kFinalizeThreads];
+  __shared__ int scor[kFinalizeThreads];
   ssum[threadIdx.x] = contrib;
+  sden[threadIdx.x] = den;
   scnt[threadIdx.x] = valid;
+  scor[threadIdx.x] = correct;
   __syncthreads();
   for (int o = kFinalizeThreads / 2; o > 0; o >>= 1) {
     if (int(threadIdx.x) < o) {
       ssum[threadIdx.x] += ssum[threadIdx.x + o];
+      sden[threadIdx.x] += sden[threadIdx.x + o];
       scnt[threadIdx.x] += scnt[threadIdx.x + o];
+      scor[threadIdx.x] += scor[threadIdx.x + o];
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     p.block_sum[blockIdx.x] = ssum[0];
+    p.block_wsum[blockIdx.x] = sden[0];
     p.block_cnt[blockIdx.x] = scnt[0];
+    p.block_correct[blockIdx.x] = scor[0];
   }
 }
 
 __global__ void __launch_bounds__(kFinalizeThreads)
     flce_finalize_loss_kernel(const FinalizeParams p, int blocks) {
   __shared__ double ssum[kFinalizeThreads];
+  __shared__ double sden[kFinalizeThreads];
   __shared__ long long scnt[kFinalizeThreads];
-  double s = 0.0;
-  long long c = 0;
+  __shared__ long long scor[kFinalizeThreads];
+  double s = 0.0, dn = 0.0;
+  long long c = 0, k = 0;
   for (int b = int(threadIdx.x); b < blocks; b += kFinalizeThreads) {
     s += p.block_sum[b];
+    dn += p.block_wsum[b];
     c += p.block_cnt[b];
+    k += p.block_correct[b];
   }
   ssum[threadIdx.x] = s;
+  sden[threadIdx.x] = dn;
   scnt[threadIdx.x] = c;
+  scor[threadIdx.x] = k;
   __syncthreads();
   for (int o = kFinalizeThreads / 2; o > 0; o >>= 1) {
     if (int(threadIdx.x) < o) {
       ssum[threadIdx.x] += ssum[threadIdx.x + o];
+      sden[threadIdx.x] += sden[threadIdx.x + o];
       scnt[threadIdx.x] += scnt[threadIdx.x + o];
+      scor[threadIdx.x] += scor[threadIdx.x + o];
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    double total = ssum[0];
-    if (p.reduction == 0) total = scnt[0] ? total / double(scnt[0]) : 0.0;
-    p.loss[0] = float(total);
+    if (p.reduction != 2) {
+      double total = ssum[0];
+      if (p.reduction == 0) total = sden[0] != 0.0 ? total / sden[0] : 0.0;
+      p.loss[0] = float(total);
+    }
+    if (p.accuracy != nullptr) p.accuracy[0] = scnt[0] ? float(double(scor[0]) / double(scnt[0])) : 0.f;
   }
 }
 
-// One block: count valid rows (16-byte vector loads of the targets), form g, then the
-// per-row coefficients {a = g(1 + 2 s lse), -lse log2e, b = g eps / V, target} the
-// gradient epilogue reads with one 16-byte load per row.
+// One block: the mean denominator (valid rows, or the sum of their target weights; 16-byte
+// vector loads of the targets), g, then the per-row coefficients the gradient epilogue
+// reads with one 16-byte load per row: {A, -lse log2e, C, target column in W or
+// kIgnoredRow} with A = g((1-eps) w_y + (eps/V) sum_j w_j + 2 s lse), C = g (1-eps) w_y,
+// and the scalar B = g eps / V.
 constexpr int kPrepThreads = 1024;
 
 __global__ void __launch_bounds__(kPrepThreads) flce_prep_kernel(const PrepParams p) {
-  __shared__ int s_cnt[kPrepThreads / 32];
+  __shared__ double s_den[kPrepThreads / 32];
   __shared__ float s_g;
   const int tid = int(threadIdx.x);
   const uintptr_t addr = reinterpret_cast<uintptr_t>(p.targets);
   const flce_vec_split sp = flce_split_for_vectors(int64_t((addr & 15u) / 4u), p.N, 4);
-  int cnt = 0;
-  for (int64_t i = tid; i < sp.head; i += kPrepThreads) cnt += (p.targets[i] != p.ignore_index);
+  auto weight_of = [&](int y) -> double {
+    if (y == p.ignore_index) return 0.0;
+    if (p.cw == nullptr || y < 0 || y >= p.V) return 1.0;
+    return double(__ldg(p.cw + y));
+  };
+  double den = 0.0;
+  for (int64_t i = tid; i < sp.head; i += kPrepThreads) den += weight_of(p.targets[i]);
   const int4* body = reinterpret_cast<const int4*>(p.targets + sp.head);
   for (int64_t i = tid; i < sp.body / 4; i += kPrepThreads) {
     const int4 v = __ldg(body + i);
-    cnt += (v.x != p.ignore_index) + (v.y != p.ignore_index) + (v.z != p.ignore_index) + (v.w != p.ignore_index);
+    den += weight_of(v.x) + weight_of(v.y) + weight_of(v.z) + weight_of(v.w);
   }
-  for (int64_t i = sp.head + sp.body + tid; i < p.N; i += kPrepThreads) cnt += (p.targets[i] != p.ignore_index);
+  for (int64_t i = sp.head + sp.body + tid; i < p.N; i += kPrepThreads) den += weight_of(p.targets[i]);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  if ((tid & 31) == 0) s_cnt[tid >> 5] = cnt;
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if ((tid & 31) == 0) s_den[tid >> 5] = den;
   __syncthreads();
   if (tid < 32) {
-    int c = s_cnt[tid];
+    double c = s_den[tid];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (tid == 0) {
       float g = *p.grad_out;
-      if (p.reduction == 0) g = c ? g / float(c) : 0.f;
+      if (p.reduction == 0) g = c != 0.0 ? float(double(g) / c) : 0.f;
       s_g = g;
-      *p.cval = g * (1.f - p.eps);
+      *p.bval = g * p.eps / float(p.V);
     }
   }
   __syncthreads();
   const float g = s_g;
-  const float b = g * p.eps / float(p.V);
+  const float wtot = p.cw != nullptr ? *p.wtot : float(p.V);
   for (int i = tid; i < p.N; i += kPrepThreads) {
     const int y = p.targets[i];
     float4 cf;
     if (y == p.ignore_index) {
-      cf = make_float4(0.f, 0.f, 0.f, __int_as_float(-1));
+      cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
     } else if (y < 0 || y >= p.V) {
       atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
-      cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(-1));
+      cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(kIgnoredRow));
     } else {
       const float l = p.lse[i];
-      cf = make_float4(g * (1.f + 2.f * p.zscale * l), -l * kLog2e, b, __int_as_float(y));
+      const float wy = p.cw != nullptr ? __ldg(p.cw + y) : 1.f;
+      const float a = g * ((1.f - p.eps) * wy + p.eps / float(p.V) * wtot + 2.f * p.zscale * l);
+      cf = make_float4(a, -l * kLog2e, g * (1.f - p.eps) * wy, __int_as_float(y - p.y_offset));
     }
     p.coef[i] = cf;
   }
+}
+
+// Sum of n floats in a fixed order (one block of 1024 threads).
+__global__ void __launch_bounds__(1024) flce_sum_kernel(const float* v, int n, float* out) {
+  __shared__ double sh[1024];
+  double s = 0.0;
+  for (int i = int(threadIdx.x); i < n; i += 1024) s += double(v[i]);
+  sh[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 512; o > 0; o >>= 1) {
+    if (int(threadIdx.x) < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = float(sh[0]);
+}
+
+// Column sums of a bf16 band: block (x, y) sums columns [256x, 256x+256) over row chunk y.
+__global__ void __launch_bounds__(256) flce_colsum_partial_kernel(const ColsumParams p) {
+  const int col = int(blockIdx.x) * 256 + int(threadIdx.x);
+  if (col >= p.cols) return;
+  const int rows_per = (p.N + p.row_chunks - 1) / p.row_chunks;
+  const int r0 = int(blockIdx.y) * rows_per;
+  const int r1 = min(p.N, r0 + rows_per);
+  float s = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const uint16_t h = p.band[size_t(r) * p.ld + col];
+    s += __uint_as_float(uint32_t(h) << 16);
+  }
+  p.partial[size_t(blockIdx.y) * p.cols + col] = s;
+}
+
+__global__ void __launch_bounds__(256) flce_colsum_final_kernel(const ColsumParams p) {
+  const int col = int(blockIdx.x) * 256 + int(threadIdx.x);
+  if (col >= p.cols) return;
+  float s = 0.f;
+  for (int c = 0; c < p.row_chunks; ++c) s += p.partial[size_t(c) * p.cols + col];
+  p.out[col] = s;
 }
 
 __global__ void flce_cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
@@ -166,13 +271,27 @@ __global__ void flce_cast_bf16_kernel(const float4* __restrict__ src, uint2* __r
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream) {
   flce_finalize_rows_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.reduction == 2) return e;
+  if (e != cudaSuccess || p.mode == FIN_SHARD_STATS || (p.reduction == 2 && p.accuracy == nullptr)) return e;
   flce_finalize_loss_kernel<<<1, kFinalizeThreads, 0, stream>>>(p, blocks);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
   flce_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream) {
+  flce_sum_kernel<<<1, 1024, 0, stream>>>(v, n, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream) {
+  const dim3 grid(unsigned((p.cols + 255) / 256), unsigned(p.row_chunks));
+  flce_colsum_partial_kernel<<<grid, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  flce_colsum_final_kernel<<<unsigned((p.cols + 255) / 256), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,7 @@ point, sizes its workspace, and refuses bad arguments before launching anything.
 
 No test here launches a kernel: the argument checks run before the device check.
 """
+import ctypes
 import json
 import os
 import re
@@ -144,3 +145,47 @@ def test_python_wrapper_validates_dtypes():
         flce.linear_cross_entropy(X, W, y)
     with pytest.raises(ValueError):
         flce.linear_cross_entropy(X.bfloat16(), W, y)  # CPU tensors are refused, never computed on the host
+
+
+def _opts(**kw):
+    return flce.make_options(**kw)
+
+
+def _fwd_ex(lib, opts, V=1024):
+    return lib.flce_forward_ex(0x10000, 0x20000, 0x30000, 256, 128, V, -100, 0.0, 0.0, 0, ctypes.byref(opts),
+                               0x40000, 0x50000, 0x60000, flce.flce_workspace_size(256, 128, V, 0), None)
+
+
+def _bwd_ex(lib, opts, V=1024):
+    return lib.flce_backward_ex(0x10000, 0x20000, 0x30000, 0x50000, 256, 128, V, -100, 0.0, 0.0, 0,
+                                ctypes.byref(opts), 0x70000, 0x80000, 0x90000, 0x60000,
+                                flce.flce_workspace_size(256, 128, V, 1), None)
+
+
+def test_option_checks(lib):
+    assert _fwd_ex(lib, _opts(softcap=-1.0)) == 1
+    assert _fwd_ex(lib, _opts(softcap=float("inf"))) == 1
+    assert _fwd_ex(lib, _opts(v_total=2048)) == 1          # forward shards go through flce_shard_stats
+    assert _fwd_ex(lib, _opts(v_offset=8)) == 1
+    assert _fwd_ex(lib, _opts(bias=0x1002)) == 2            # misaligned
+    assert _bwd_ex(lib, _opts(dbias=0xA0000)) == 1          # dbias needs a bias
+    assert _bwd_ex(lib, _opts(v_offset=1000, v_total=1500)) == 1  # shard beyond the vocabulary
+    assert _bwd_ex(lib, _opts(bias=0xA0000, v_offset=0, v_total=4096)) == 1  # shards take no bias
+    assert _bwd_ex(lib, _opts(dX_f32=0xA0008)) == 2         # fp32 dX needs 16-byte alignment
+    assert lib.flce_combine_shards(0x10000, 0, 0x30000, 256, 1024, -100, 0.0, 0.0, 0, 0x40000, 0x50000,
+                                   0x60000, 1 << 20, None) == 1   # K >= 1
+    assert lib.flce_shard_stats(0x10000, 0x20000, 0x30000, 256, 128, 1024, -8, -100, 0x40000, 0x60000,
+                                1 << 20, None) == 1         # negative offset
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the refusal on a machine without a GB300")
+def test_extended_entry_points_refuse_without_a_device(lib):
+    assert _fwd_ex(lib, _opts(softcap=30.0)) == 3
+    assert _bwd_ex(lib, _opts(v_offset=0, v_total=2048)) == 3
+
+
+def test_fused_workspace_is_the_larger_of_the_two():
+    for (n, d, v) in [(256, 128, 1024), (4096, 2048, 32000), (16, 8, 65536)]:
+        f = flce.flce_workspace_size(n, d, v, 0)
+        b = flce.flce_workspace_size(n, d, v, 1)
+        assert flce.flce_workspace_size(n, d, v, 2) == max(f, b)

@@ -140,7 +140,7 @@ def kernel_launches_per_step(N, D, V, reduction):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
     backward prep + 3 GEMMs per vocabulary band + the dX cast."""
     kBN = 256
-    vc = max(kBN, ((1 << 30) // (2 * N)) // kBN * kBN)
+    vc = max(kBN, min(16384, ((1 << 30) // (2 * N)) // kBN * kBN))
     half = (((V + 1) // 2) + kBN - 1) // kBN * kBN
     vc = min(vc, half)
     bands = -(-V // vc)

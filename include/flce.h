@@ -151,6 +151,10 @@ typedef struct flce_options {
   float* dX_f32;             /* backward out: device fp32 [N, D] dX written instead of the bf16 dX, or NULL */
   int64_t v_offset;          /* vocabulary shard: global index of W's first column (0 if unsharded) */
   int64_t v_total;           /* vocabulary shard: size of the full vocabulary (0 means V: unsharded) */
+  int64_t row_band;          /* backward: > 0 processes rows in bands of this many ([P1] "Path to
+                                Production": micro-batching along N), so the workspace is
+                                flce_workspace_size(row_band, D, V, 1) whatever N is; dW then
+                                accumulates across bands (fp32 adds in a fixed order). 0: all rows. */
 } flce_options;
 
 /* flce_forward with options (NULL behaves exactly like flce_forward). Vocabulary

@@ -50,8 +50,8 @@ struct FwdLayout {
 };
 
 // Header words of every workspace: [0] device error word, [16] B = g eps / V (backward),
-// [24] sum of the class weights.
-constexpr size_t kHdrErr = 0, kHdrB = 16, kHdrWtot = 24;
+// [24] sum of the class weights, [28] g (backward).
+constexpr size_t kHdrErr = 0, kHdrB = 16, kHdrWtot = 24, kHdrG = 28;
 
 FwdLayout fwd_layout(int64_t N, int64_t V) {
   FwdLayout L{};
@@ -81,11 +81,15 @@ struct BwdLayout {
   int64_t Vc;
 };
 
-// Width of the gradient band: as many 256-column tiles as fit in the byte budget,
-// and never more than half the vocabulary (rounded up to a tile), so that no buffer
-// holds N x V values once V exceeds one tile.
+// Width of the gradient band: as many 256-column tiles as fit in the byte budget, at
+// most kMaxBandCols (wider bands measured no faster and cost memory), and never more
+// than half the vocabulary (rounded up to a tile), so that no buffer holds N x V values
+// once V exceeds one tile.
+constexpr int64_t kMaxBandCols = 16384;
+
 int64_t band_width(int64_t N, int64_t D, int64_t V) {
   int64_t vc = (kGradBandBudget / (2 * N)) / kBN * kBN;
+  if (vc > kMaxBandCols) vc = kMaxBandCols;
   if (FLCE_BAND_W_L2_BYTES > 0) {
     const int64_t l2 = (FLCE_BAND_W_L2_BYTES / (2 * D)) / kBN * kBN;
     if (l2 < vc) vc = l2;
@@ -272,6 +276,7 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
       (o->dbias && !aligned(o->dbias, 4)) || (o->dX_f32 && !aligned(o->dX_f32, 16)))
     return FLCE_ERR_ALIGNMENT;
   if (o->dbias && !o->bias) return FLCE_ERR_INVALID_ARG;
+  if (o->row_band < 0) return FLCE_ERR_INVALID_ARG;
   const bool shard = o->v_total != 0 && o->v_total != pb.V;
   if (shard) {
     if (!backward) return FLCE_ERR_INVALID_ARG;  // forward shards go through flce_shard_stats
@@ -367,15 +372,23 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   return FLCE_OK;
 }
 
+// Rows handled per backward pass: all of them, or bands of opt->row_band.
+int64_t backward_rows(const flce_options* opt, int64_t N) {
+  return (opt && opt->row_band > 0 && opt->row_band < N) ? opt->row_band : N;
+}
+
 flce_status run_backward(const Problem& pb, const flce_options* opt, const float* lse, const float* grad_out,
                          void* dX, float* dW, uint8_t* ws, bool clear_header, int sms, cudaStream_t stream) {
-  const BwdLayout L = bwd_layout(pb.N, pb.D, pb.V);
+  const int64_t Nb = backward_rows(opt, pb.N);
+  const BwdLayout L = bwd_layout(Nb, pb.D, pb.V);
   int* err = reinterpret_cast<int*>(ws + kHdrErr);
   float* bval = reinterpret_cast<float*>(ws + kHdrB);
   float* wtot = reinterpret_cast<float*>(ws + kHdrWtot);
+  float* gval = reinterpret_cast<float*>(ws + kHdrG);
   float4* coef = reinterpret_cast<float4*>(ws + L.coef);
   void* band = ws + L.band;
-  float* dx_f32 = (opt && opt->dX_f32) ? opt->dX_f32 : reinterpret_cast<float*>(ws + L.dx_acc);
+  float* dx_acc = reinterpret_cast<float*>(ws + L.dx_acc);
+  const bool f32_out = opt && opt->dX_f32;
   const int64_t Vc = L.Vc;
   const bool shard = opt && opt->v_total != 0 && opt->v_total != pb.V;
   const int64_t V_total = shard ? opt->v_total : pb.V;
@@ -383,25 +396,15 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const float* cw = opt ? opt->class_weight : nullptr;
   const bool ext = opt_ext_grad(opt);
 
-  CUtensorMap tmXk, tmXmn, tmWmn, tmWk, tmG, tmGmn, tmDW, tmDX;
-  const bool enc =
-      encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64,
-                kBM) &&
-      encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64,
-                64) &&
-      encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64,
-                64) &&
-      encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64,
-                uint32_t(gemm_b_rows_per_cta())) &&
-      encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(pb.N), uint64_t(Vc), 64,
-                kBM) &&
-      encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(pb.N), uint64_t(Vc), 64,
-                64) &&
-      encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 32,
-                kBM) &&
-      encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_f32, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
-                32, kBM);
-  if (!enc) return FLCE_ERR_CUDA;
+  // maps that do not depend on the row band
+  CUtensorMap tmWmn, tmWk, tmDW;
+  if (!encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
+                 64, 64) ||
+      !encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
+                 64, uint32_t(gemm_b_rows_per_cta())) ||
+      !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 32,
+                 kBM))
+    return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
   if (cw) FLCE_CUDA_CHECK(launch_sum(cw, int(pb.V), wtot, stream));
@@ -419,65 +422,92 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   pp.cw = cw;
   pp.wtot = wtot;
   pp.coef = coef;
+  pp.gval = gval;
   pp.bval = bval;
   pp.err = err;
-  FLCE_CUDA_CHECK(launch_prep(pp, stream));
+  FLCE_CUDA_CHECK(launch_denominator(pp, stream));  // g over every row of the batch
 
-  const int64_t n_tiles = cdiv(pb.N, gemm_tile_rows());
   const int64_t d_tiles_m = cdiv(pb.D, gemm_tile_rows());  // dW rows
   const int64_t d_tiles_n = cdiv(pb.D, kBN);               // dX columns
-  for (int64_t v0 = 0, band_i = 0; v0 < pb.V; v0 += Vc, ++band_i) {
-    const int64_t vc = (pb.V - v0 < Vc) ? pb.V - v0 : Vc;
-    const int64_t vt = cdiv(vc, kBN);
+  for (int64_t n0 = 0; n0 < pb.N; n0 += Nb) {
+    const int64_t nb = (pb.N - n0 < Nb) ? pb.N - n0 : Nb;
+    const void* Xb = static_cast<const uint8_t*>(pb.X) + size_t(n0) * size_t(pb.D) * 2;
+    float* dx_dst = f32_out ? opt->dX_f32 + size_t(n0) * size_t(pb.D) : dx_acc;
+    CUtensorMap tmXk, tmXmn, tmG, tmGmn, tmDX;
+    const bool enc =
+        encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
+                  kBM) &&
+        encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
+                  64) &&
+        encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
+                  kBM) &&
+        encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
+                  64) &&
+        encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_dst, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D),
+                  32, kBM);
+    if (!enc) return FLCE_ERR_CUDA;
+    PrepParams pb_rows = pp;
+    pb_rows.targets = pb.targets + n0;
+    pb_rows.lse = lse + n0;
+    FLCE_CUDA_CHECK(launch_coef(pb_rows, int(nb), stream));
 
-    WalkParams wg{};
-    wg.total_tiles = int(n_tiles * vt);
-    wg.tiles_minor = int(vt);
-    wg.num_kb = int(cdiv(pb.D, kBK));
-    wg.b_row_off = int(v0);
-    GradEpiParams ge{};
-    ge.coef = coef;
-    ge.bval = bval;
-    ge.N = int(pb.N);
-    ge.V = int(pb.V);
-    ge.chunk_v0 = int(v0);
-    ge.err = err;
-    if (ext) {
-      ge.bias = opt->bias;
-      ge.cw = cw;
-      ge.softcap = opt->softcap;
+    const int64_t n_tiles = cdiv(nb, gemm_tile_rows());
+    for (int64_t v0 = 0, band_i = 0; v0 < pb.V; v0 += Vc, ++band_i) {
+      const int64_t vc = (pb.V - v0 < Vc) ? pb.V - v0 : Vc;
+      const int64_t vt = cdiv(vc, kBN);
+
+      WalkParams wg{};
+      wg.total_tiles = int(n_tiles * vt);
+      wg.tiles_minor = int(vt);
+      wg.num_kb = int(cdiv(pb.D, kBK));
+      wg.b_row_off = int(v0);
+      GradEpiParams ge{};
+      ge.coef = coef;
+      ge.bval = bval;
+      ge.N = int(nb);
+      ge.V = int(pb.V);
+      ge.chunk_v0 = int(v0);
+      ge.err = err;
+      if (ext) {
+        ge.bias = opt->bias;
+        ge.cw = cw;
+        ge.softcap = opt->softcap;
+      }
+      FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, ext, stream));
+
+      if (opt && opt->dbias) {
+        ColsumParams cp{};
+        cp.band = static_cast<const uint16_t*>(band);
+        cp.N = int(nb);
+        cp.ld = int(Vc);
+        cp.cols = int(vc);
+        cp.row_chunks = kColsumChunks;
+        cp.partial = reinterpret_cast<float*>(ws + L.colsum);
+        cp.out = opt->dbias + v0;
+        cp.accumulate = n0 > 0 ? 1 : 0;
+        FLCE_CUDA_CHECK(launch_colsum(cp, stream));
+      }
+
+      WalkParams ww{};
+      ww.total_tiles = int(vt * d_tiles_m);
+      ww.tiles_minor = int(d_tiles_m);
+      ww.num_kb = int(cdiv(nb, kBK));
+      StoreEpiParams sw{n0 > 0 ? 1 : 0, int(v0), err};  // later row bands add into dW
+      FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
+
+      WalkParams wx{};
+      wx.total_tiles = int(n_tiles * d_tiles_n);
+      wx.tiles_minor = int(d_tiles_n);
+      wx.num_kb = int(cdiv(vc, kBK));
+      wx.b_k0 = int(v0);
+      StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
+      FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx, stream));
     }
-    FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, ext, stream));
-
-    if (opt && opt->dbias) {
-      ColsumParams cp{};
-      cp.band = static_cast<const uint16_t*>(band);
-      cp.N = int(pb.N);
-      cp.ld = int(Vc);
-      cp.cols = int(vc);
-      cp.row_chunks = kColsumChunks;
-      cp.partial = reinterpret_cast<float*>(ws + L.colsum);
-      cp.out = opt->dbias + v0;
-      FLCE_CUDA_CHECK(launch_colsum(cp, stream));
+    if (!f32_out) {
+      void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;
+      FLCE_CUDA_CHECK(launch_cast_bf16(dx_acc, dXb, size_t(nb) * size_t(pb.D), sms, stream));
     }
-
-    WalkParams ww{};
-    ww.total_tiles = int(vt * d_tiles_m);
-    ww.tiles_minor = int(d_tiles_m);
-    ww.num_kb = int(cdiv(pb.N, kBK));
-    StoreEpiParams sw{0, int(v0), err};
-    FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
-
-    WalkParams wx{};
-    wx.total_tiles = int(n_tiles * d_tiles_n);
-    wx.tiles_minor = int(d_tiles_n);
-    wx.num_kb = int(cdiv(vc, kBK));
-    wx.b_k0 = int(v0);
-    StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
-    FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx, stream));
   }
-  if (!(opt && opt->dX_f32))
-    FLCE_CUDA_CHECK(launch_cast_bf16(dx_f32, dX, size_t(pb.N) * size_t(pb.D), sms, stream));
   return FLCE_OK;
 }
 
@@ -535,7 +565,7 @@ flce_status flce_backward_ex(const void* X, const void* W, const int32_t* target
   const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, true)) != FLCE_OK) return st;
-  if (ws_bytes < bwd_layout(N, D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < bwd_layout(backward_rows(opt, N), D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   int sms = 0;
   if ((st = current_device(&sms)) != FLCE_OK) return st;
   return run_backward(pb, opt, lse, grad_out, dX, dW, static_cast<uint8_t*>(workspace), true, sms,
@@ -561,7 +591,10 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
-  if (ws_bytes < flce_workspace_size(N, D, V, 2)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  {
+    const size_t f = fwd_layout(N, V).total, b = bwd_layout(backward_rows(opt, N), D, V).total;
+    if (ws_bytes < (f > b ? f : b)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  }
   int sms = 0;
   if ((st = current_device(&sms)) != FLCE_OK) return st;
   const int units = forward_max_units();

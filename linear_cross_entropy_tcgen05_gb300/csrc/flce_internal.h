@@ -128,7 +128,8 @@ struct PrepParams {
   const float* cw;      // [V] class weights or null
   const float* wtot;    // device scalar sum_j w_j (with cw)
   float4* coef;
-  float* bval;
+  float* gval;          // device scalar g (written by the denominator pass)
+  float* bval;          // device scalar B = g eps / V
   int* err;
 };
 
@@ -138,6 +139,7 @@ struct ColsumParams {
   int row_chunks;
   float* partial;        // [row_chunks][cols]
   float* out;            // [cols]
+  int accumulate;        // add to out instead of overwriting
 };
 
 // Rows of one GEMM output tile (a CTA pair: 2 x 128).
@@ -151,7 +153,10 @@ int forward_max_units();
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
                                 cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream);
-cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream);
+// g and B from the mean denominator over all rows (one block).
+cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream);
+// Per-row gradient coefficients of rows [0, n_rows) of p.targets / p.lse into p.coef.
+cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream);
 // out[0] = sum of v[0..n) in a fixed order (one block).
 cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream);
 // Column sums of a bf16 band, fixed order (two kernels).

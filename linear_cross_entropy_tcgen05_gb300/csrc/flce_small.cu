@@ -158,15 +158,12 @@ __global__ void __launch_bounds__(kFinalizeThreads)
 }
 
 // One block: the mean denominator (valid rows, or the sum of their target weights; 16-byte
-// vector loads of the targets), g, then the per-row coefficients the gradient epilogue
-// reads with one 16-byte load per row: {A, -lse log2e, C, target column in W or
-// kIgnoredRow} with A = g((1-eps) w_y + (eps/V) sum_j w_j + 2 s lse), C = g (1-eps) w_y,
-// and the scalar B = g eps / V.
+// vector loads of the targets) over all N rows, then g and the scalar B = g eps / V in the
+// workspace header.
 constexpr int kPrepThreads = 1024;
 
-__global__ void __launch_bounds__(kPrepThreads) flce_prep_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(kPrepThreads) flce_denominator_kernel(const PrepParams p) {
   __shared__ double s_den[kPrepThreads / 32];
-  __shared__ float s_g;
   const int tid = int(threadIdx.x);
   const uintptr_t addr = reinterpret_cast<uintptr_t>(p.targets);
   const flce_vec_split sp = flce_split_for_vectors(int64_t((addr & 15u) / 4u), p.N, 4);
@@ -194,29 +191,35 @@ __global__ void __launch_bounds__(kPrepThreads) flce_prep_kernel(const PrepParam
     if (tid == 0) {
       float g = *p.grad_out;
       if (p.reduction == 0) g = c != 0.0 ? float(double(g) / c) : 0.f;
-      s_g = g;
+      *p.gval = g;
       *p.bval = g * p.eps / float(p.V);
     }
   }
-  __syncthreads();
-  const float g = s_g;
+}
+
+// Per-row coefficients for rows [0, n_rows) of `targets` / `lse` (a band of the batch):
+// {A, -lse log2e, C, target column in W or kIgnoredRow} with
+// A = g((1-eps) w_y + (eps/V) sum_j w_j + 2 s lse), C = g (1-eps) w_y; one 16-byte load per
+// row in the gradient epilogue.
+__global__ void __launch_bounds__(256) flce_coef_kernel(const PrepParams p, int n_rows) {
+  const int i = int(blockIdx.x) * 256 + int(threadIdx.x);
+  if (i >= n_rows) return;
+  const float g = *p.gval;
   const float wtot = p.cw != nullptr ? *p.wtot : float(p.V);
-  for (int i = tid; i < p.N; i += kPrepThreads) {
-    const int y = p.targets[i];
-    float4 cf;
-    if (y == p.ignore_index) {
-      cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
-    } else if (y < 0 || y >= p.V) {
-      atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
-      cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(kIgnoredRow));
-    } else {
-      const float l = p.lse[i];
-      const float wy = p.cw != nullptr ? __ldg(p.cw + y) : 1.f;
-      const float a = g * ((1.f - p.eps) * wy + p.eps / float(p.V) * wtot + 2.f * p.zscale * l);
-      cf = make_float4(a, -l * kLog2e, g * (1.f - p.eps) * wy, __int_as_float(y - p.y_offset));
-    }
-    p.coef[i] = cf;
+  const int y = p.targets[i];
+  float4 cf;
+  if (y == p.ignore_index) {
+    cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
+  } else if (y < 0 || y >= p.V) {
+    atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
+    cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(kIgnoredRow));
+  } else {
+    const float l = p.lse[i];
+    const float wy = p.cw != nullptr ? __ldg(p.cw + y) : 1.f;
+    const float a = g * ((1.f - p.eps) * wy + p.eps / float(p.V) * wtot + 2.f * p.zscale * l);
+    cf = make_float4(a, -l * kLog2e, g * (1.f - p.eps) * wy, __int_as_float(y - p.y_offset));
   }
+  p.coef[i] = cf;
 }
 
 // Sum of n floats in a fixed order (one block of 1024 threads).
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(256) flce_colsum_partial_kernel(const ColsumPa
 __global__ void __launch_bounds__(256) flce_colsum_final_kernel(const ColsumParams p) {
   const int col = int(blockIdx.x) * 256 + int(threadIdx.x);
   if (col >= p.cols) return;
-  float s = 0.f;
+  float s = p.accumulate ? p.out[col] : 0.f;
   for (int c = 0; c < p.row_chunks; ++c) s += p.partial[size_t(c) * p.cols + col];
   p.out[col] = s;
 }
@@ -276,8 +279,13 @@ cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st
   return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const PrepParams& p, cudaStream_t stream) {
-  flce_prep_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream) {
+  flce_denominator_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream) {
+  flce_coef_kernel<<<unsigned((n_rows + 255) / 256), 256, 0, stream>>>(p, n_rows);
   return cudaGetLastError();
 }
 

@@ -207,3 +207,43 @@ def test_vocabulary_shards_match_the_whole(gpu_lib, cuts, eps, s, red):
         assert np.max(np.abs(st[0] - lse_k)) <= TOL_LSE_ABS
         assert np.array_equal(st[3], own_k)
         assert np.max(np.abs(st[2] - zy_k)) <= 1e-3
+
+
+@pytest.mark.parametrize("row_band,opts", [(300, {}), (256, {"cw": True}), (512, {"bias": True, "softcap": 8.0})])
+def test_row_band_backward_matches_the_oracle(gpu_lib, row_band, opts):
+    """Micro-batching along N: the backward in bands of rows, with a workspace sized for one band."""
+    wl = custom("bands", 1000, 136, 4104, seed=36, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-3)
+    X, W, y, bias, cw = _inputs(wl)
+    N, D, V = wl.N, wl.D, wl.V
+    b = bias if opts.get("bias") else None
+    w = cw if opts.get("cw") else None
+    softcap = opts.get("softcap", 0.0)
+    Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
+    bd = b.to(DEV) if b is not None else None
+    wd = w.to(DEV) if w is not None else None
+    common = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean")
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    flce.flce_forward_ex(Xd, Wd, yd, loss, lse, _ws(N, D, V, 0), *common,
+                         options=flce.make_options(softcap=softcap, bias=bd, class_weight=wd))
+    ws = _ws(row_band, D, V, 1)  # one band's workspace
+    assert ws.numel() < flce.flce_workspace_size(N, D, V, 1)
+    dX = torch.empty(N, D, dtype=torch.bfloat16, device=DEV)
+    dW = torch.empty(D, V, device=DEV)
+    dbias = torch.empty(V, device=DEV) if b is not None else None
+    g = torch.ones(1, device=DEV)
+    flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, ws, *common,
+                          options=flce.make_options(softcap=softcap, bias=bd, class_weight=wd, dbias=dbias,
+                                                    row_band=row_band))
+    assert flce.flce_check_device_error(ws) == 0
+    torch.cuda.synchronize()
+    _, _, ref_dX, ref_dW, ref_db = oracle.forward_backward_ext(X, W, y, *common, softcap=softcap, bias=b,
+                                                               class_weight=w)
+    assert rel_fro(dX.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
+    assert rel_fro(dW.cpu().numpy(), ref_dW) <= TOL_DW_REL
+    if b is not None:
+        assert rel_fro(dbias.cpu().numpy(), ref_db) <= TOL_DW_REL
+    # too small a workspace for the band is refused
+    small = _ws(row_band // 2, D, V, 1)
+    st = flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, small, *common, raise_on_error=False,
+                               options=flce.make_options(row_band=row_band))
+    assert st == 4

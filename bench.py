@@ -138,14 +138,14 @@ def barrier(world: int):
 
 def kernel_launches_per_step(N, D, V, reduction):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
-    backward prep + 3 GEMMs per vocabulary band + the dX cast."""
+    backward denominator + row coefficients + 3 GEMMs per vocabulary band + the dX cast."""
     kBN = 256
     vc = max(kBN, min(16384, ((1 << 30) // (2 * N)) // kBN * kBN))
     half = (((V + 1) // 2) + kBN - 1) // kBN * kBN
     vc = min(vc, half)
     bands = -(-V // vc)
     fwd = 1 + 1 + (0 if reduction == "none" else 1)
-    bwd = 1 + 3 * bands + 1
+    bwd = 2 + 3 * bands + 1
     return fwd + bwd, bands, vc
 
 

@@ -279,22 +279,28 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
     """loss = CE(softmax(X @ W), targets) with fused tensor-core kernels (no N x V logits)."""
 
     @staticmethod
-    def forward(ctx, X, W, targets, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean"):
+    def forward(ctx, X, W, targets, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",
+                softcap=0.0, bias=None, class_weight=None):
         _validate(X, W, targets)
         N, D = X.shape
         V = W.shape[1]
         ws = _workspace(N, D, V, X.device, False)
         loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
         lse = torch.empty(N, dtype=torch.float32, device=X.device)
-        flce_forward(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction)
+        b32 = bias.detach().float().contiguous() if bias is not None else None
+        w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32)
+        flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction, opts)
         ctx.save_for_backward(X, W, targets, lse)
-        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction)
+        ctx.extra = (b32, w32, bias is not None and bias.requires_grad, bias.dtype if bias is not None else None)
+        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction, softcap)
         return loss if reduction == "none" else loss[0]
 
     @staticmethod
     def backward(ctx, grad_loss):
         X, W, targets, lse = ctx.saved_tensors
-        ignore_index, label_smoothing, zloss_scale, reduction = ctx.opts
+        b32, w32, want_db, b_dtype = ctx.extra
+        ignore_index, label_smoothing, zloss_scale, reduction, softcap = ctx.opts
         if reduction == "none":
             raise RuntimeError("reduction='none' has no fused backward (FLCE_ERR_REDUCTION_NONE_GRAD)")
         N, D = X.shape
@@ -303,15 +309,23 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         g = grad_loss.detach().to(device=X.device, dtype=torch.float32).reshape(1).contiguous()
         dX = torch.empty_like(X)
         dW = torch.empty(D, V, dtype=torch.float32, device=X.device)
-        flce_backward(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction)
-        return dX, dW.to(W.dtype), None, None, None, None, None
+        db = torch.empty(V, dtype=torch.float32, device=X.device) if want_db else None
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db)
+        flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction,
+                         opts)
+        return (dX, dW.to(W.dtype), None, None, None, None, None, None,
+                db.to(b_dtype) if db is not None else None, None)
 
 
 def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,
-                         zloss_scale: float = 0.0, reduction: str = "mean"):
+                         zloss_scale: float = 0.0, reduction: str = "mean", softcap: float = 0.0, bias=None,
+                         class_weight=None):
     """Fused linear cross-entropy of X [N,D] (bf16), W [D,V] (bf16), int32 targets [N].
 
-    The gradient of W is accumulated in fp32 by the kernels and returned in W's dtype
-    through autograd; call ``flce_backward`` directly to keep the fp32 dW.
+    Optional: a logit ``softcap``, a ``bias`` [V] (its gradient is returned through
+    autograd) and per-class weights ``class_weight`` [V]. The gradient of W is
+    accumulated in fp32 by the kernels and returned in W's dtype through autograd; call
+    ``flce_backward`` directly to keep the fp32 dW.
     """
-    return LinearCrossEntropyFunction.apply(X, W, targets, ignore_index, label_smoothing, zloss_scale, reduction)
+    return LinearCrossEntropyFunction.apply(X, W, targets, ignore_index, label_smoothing, zloss_scale, reduction,
+                                            softcap, bias, class_weight)

@@ -1,0 +1,49 @@
+"""The benchmark's multi-rank plumbing on CPU: two gloo ranks agree on the maximum
+elapsed time and pass the barrier (each rank runs its own replica; there is no
+collective on the data path)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    import bench
+    w, r, _ = bench.dist_setup(world)
+    assert (w, r) == (world, rank)
+    bench.barrier(w)
+    out[rank] = bench.max_over_ranks(10.0 * (rank + 1), w)
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max_time():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert dict(out) == {0: 20.0, 1: 20.0}
+
+
+def test_launch_count_matches_the_band_schedule():
+    import bench
+    total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean")
+    assert (bands, vc) == (16, 8192) and total == 3 + 2 + 3 * 16 + 1

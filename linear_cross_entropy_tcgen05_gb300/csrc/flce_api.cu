@@ -35,7 +35,7 @@ namespace {
 #define FLCE_BAND_W_L2_BYTES int64_t(0)  // if > 0: also cap the band so its W slice (2*D*Vc) fits this
 #endif
 #ifndef FLCE_FWD_GN
-#define FLCE_FWD_GN 0  // forward row tiles per group; 0 chooses from the resident CTA pairs
+#define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
 #endif
 
 constexpr size_t kHeaderBytes = 256;
@@ -191,7 +191,7 @@ flce_status check_common(const void* X, const void* W, const int32_t* targets, i
   return FLCE_OK;
 }
 
-// Forward grid: gN row tiles x S vocabulary ranges = the resident CTA pairs.
+// Forward grid: gN row blocks x S vocabulary ranges = the resident CTA pairs.
 void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc, int* gN_out, int* S_out) {
   int gN = 1;
   const int cands[4] = {8, 4, 2, 1};
@@ -201,7 +201,8 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
       break;
     }
   if (FLCE_FWD_GN > 0 && FLCE_FWD_GN <= units) gN = FLCE_FWD_GN;
-  if (gN > n_tiles) gN = int(n_tiles);
+  const int64_t row_blocks = cdiv(n_tiles, kFwdRowBlock);
+  if (gN > row_blocks) gN = int(row_blocks);
   int64_t S = units / gN;
   if (S > v_tiles) S = v_tiles;
   if (S > S_alloc) S = S_alloc;

@@ -68,6 +68,7 @@ struct Tile {
   int b_k0;    // ... and in B
   int num_kb;  // number of 64-wide K blocks
   int aux;     // forward: vocabulary range index of the partial statistics
+  int sub;     // forward: row tile within the row block
   int flags;
 };
 
@@ -90,17 +91,19 @@ __device__ __forceinline__ Pair pair_id() {
 // Tile schedules (every role of both CTAs of a pair walks the same sequence)
 // ---------------------------------------------------------------------------------
 
-// Forward: the clusters form gN row tiles x S vocabulary ranges. Cluster c keeps
-// row-tile offset c % gN and walks groups of gN row tiles; in group g it covers
-// vocabulary range (c / gN + g) mod S, so the extra tile of the longer ranges rotates
-// among clusters. Running statistics stay in registers across a range and are written
-// once per (row, range).
+// Forward: the clusters form gN row blocks x S vocabulary ranges; a row block is
+// kFwdRowBlock row tiles. Cluster c keeps row-block offset c % gN and walks groups of gN
+// row blocks; in group g it covers vocabulary range (c / gN + g) mod S, so the extra tile
+// of the longer ranges rotates among clusters. For every vocabulary tile of its range the
+// cluster computes the tiles of all row tiles of its block back to back, so each W tile
+// is streamed from HBM once per row block and re-read from L2 right away. Running
+// statistics stay in registers (one set per row tile of the block) and are written once
+// per (row, range).
 template <int CG>
 struct FwdSched {
   int n_tiles, v_tiles, gN, S, num_kb;
   int n_off, split, rank;
-  int g, vt, vt_end, range, n_tile;
-  bool first;
+  int g, vt, vt0, vt_end, range, rb0, rb_tiles, j;
 
   __device__ explicit FwdSched(const FwdParams& p) : n_tiles(p.n_tiles), v_tiles(p.v_tiles), gN(p.gN), S(p.S),
                                                      num_kb(p.num_kb) {
@@ -109,30 +112,33 @@ struct FwdSched {
     split = pr.cid / gN;
     rank = pr.rank;
     g = -1;
-    vt = vt_end = range = n_tile = 0;
-    first = false;
+    vt = vt0 = vt_end = range = rb0 = rb_tiles = j = 0;
   }
 
   __device__ bool next(Tile& t) {
     if (vt >= vt_end) {
       ++g;
-      n_tile = g * gN + n_off;
-      if (n_tile >= n_tiles) return false;
+      rb0 = (g * gN + n_off) * kFwdRowBlock;
+      if (rb0 >= n_tiles) return false;
+      rb_tiles = n_tiles - rb0 < kFwdRowBlock ? n_tiles - rb0 : kFwdRowBlock;
       range = (split + g) % S;
-      vt = int((long long)range * v_tiles / S);
+      vt0 = vt = int((long long)range * v_tiles / S);
       vt_end = int((long long)(range + 1) * v_tiles / S);
       if (vt >= vt_end) return false;  // S <= v_tiles on the host, so never taken
-      first = true;
+      j = 0;
     }
-    t.a_row = n_tile * Geo<CG>::kTileRows + rank * kBM;
+    t.a_row = (rb0 + j) * Geo<CG>::kTileRows + rank * kBM;
     t.b_row = vt * kBN;
     t.a_k0 = 0;
     t.b_k0 = 0;
     t.num_kb = num_kb;
     t.aux = range;
-    t.flags = (first ? TILE_FIRST : 0) | (vt + 1 == vt_end ? TILE_LAST : 0);
-    first = false;
-    ++vt;
+    t.sub = j;
+    t.flags = (vt == vt0 ? TILE_FIRST : 0) | (vt + 1 == vt_end ? TILE_LAST : 0);
+    if (++j == rb_tiles) {
+      j = 0;
+      ++vt;
+    }
     return true;
   }
 };
@@ -164,6 +170,7 @@ struct WalkSched {
     t.b_k0 = w.b_k0;
     t.num_kb = w.num_kb;
     t.aux = 0;
+    t.sub = 0;
     t.flags = TILE_FIRST | TILE_LAST;
     i += step;
     return true;
@@ -257,30 +264,56 @@ __device__ __forceinline__ void tmem_teardown(uint32_t tmem_base, int warp) {
   }
 }
 
-template <int CG, bool A_MN, bool B_MN>
+// L2 policies of the operands of each GEMM: the operand that every tile of a launch
+// re-reads (W in the backward GEMMs) stays, the streamed one goes first.
+template <int KIND>
+struct OperandPolicy {
+  static constexpr int A = FLCE_L2_HINTS && KIND == WALK_DX ? POL_EVICT_FIRST : POL_NORMAL;
+  static constexpr int B = FLCE_L2_HINTS && (KIND == WALK_GRAD || KIND == WALK_DX) ? POL_EVICT_LAST : POL_NORMAL;
+  static constexpr int STORE = FLCE_L2_HINTS && KIND == WALK_GRAD ? POL_EVICT_FIRST : POL_NORMAL;
+};
+constexpr int KIND_FWD = -1;
+template <>
+struct OperandPolicy<KIND_FWD> {
+  static constexpr int A = FLCE_L2_HINTS ? POL_EVICT_LAST : POL_NORMAL;  // the row block's X tiles
+  static constexpr int B = POL_NORMAL;
+  static constexpr int STORE = POL_NORMAL;
+};
+
+template <int CG, bool A_MN, bool B_MN, int KIND>
 __device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUtensorMap* tma, const CUtensorMap* tmb,
                                            uint64_t* bar_local, uint32_t bar_leader, const Tile& t, int kb,
-                                           int rank) {
+                                           int rank, uint64_t pol_a, uint64_t pol_b) {
   const int ka = t.a_k0 + kb * kBK;
   const int kbb = t.b_k0 + kb * kBK;
   const int b0 = t.b_row + rank * Geo<CG>::kBRows;
-  auto load = [&](void* dst, const CUtensorMap* m, int x, int y) {
-    if (CG == 1)
-      tma_load_2d(dst, m, bar_local, x, y);
-    else
-      tma_load_2d_pair(dst, m, bar_leader, x, y);
+  auto load = [&](void* dst, const CUtensorMap* m, int x, int y, bool hint, uint64_t pol) {
+    if (CG == 1) {
+      if (hint)
+        tma_load_2d_hint(dst, m, bar_local, x, y, pol);
+      else
+        tma_load_2d(dst, m, bar_local, x, y);
+    } else {
+      if (hint)
+        tma_load_2d_pair_hint(dst, m, bar_leader, x, y, pol);
+      else
+        tma_load_2d_pair(dst, m, bar_leader, x, y);
+    }
   };
+  constexpr bool ha = OperandPolicy<KIND>::A != POL_NORMAL;
+  constexpr bool hb = OperandPolicy<KIND>::B != POL_NORMAL;
   if (!A_MN) {
-    load(sa, tma, ka, t.a_row);  // box {64 K, 128 rows}
+    load(sa, tma, ka, t.a_row, ha, pol_a);  // box {64 K, 128 rows}
   } else {
 #pragma unroll
-    for (int j = 0; j < kBM / 64; ++j) load(sa + j * 8192, tma, t.a_row + 64 * j, ka);  // {64 M, 64 K}
+    for (int j = 0; j < kBM / 64; ++j) load(sa + j * 8192, tma, t.a_row + 64 * j, ka, ha, pol_a);  // {64 M, 64 K}
   }
   if (!B_MN) {
-    load(sb, tmb, kbb, b0);  // box {64 K, 256/CG rows}
+    load(sb, tmb, kbb, b0, hb, pol_b);  // box {64 K, 256/CG rows}
   } else {
 #pragma unroll
-    for (int j = 0; j < Geo<CG>::kBRows / 64; ++j) load(sb + j * 8192, tmb, b0 + 64 * j, kbb);  // {64 N, 64 K}
+    for (int j = 0; j < Geo<CG>::kBRows / 64; ++j)
+      load(sb + j * 8192, tmb, b0 + 64 * j, kbb, hb, pol_b);  // {64 N, 64 K}
   }
 }
 
@@ -309,10 +342,12 @@ __device__ __forceinline__ void commit_both(uint64_t* bar) {
     tc_commit_pair_multicast(bar, uint16_t(0x3));
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, class Sched, class SP>
+template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
 __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* tma, const CUtensorMap* tmb,
                                               const SP& sp, const WaitCtx& w, int rank) {
   Sched sched(sp);
+  const uint64_t pol_a = make_l2_policy<OperandPolicy<KIND>::A>();
+  const uint64_t pol_b = make_l2_policy<OperandPolicy<KIND>::B>();
   Tile t;
   int stage = 0;
   uint32_t phase = 0;
@@ -325,7 +360,8 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
       if (leader) mbar_arrive_expect_tx(&s.full[stage], Geo<CG>::kTxBytes);
       uint8_t* sa = s.stage + stage * Geo<CG>::kStageBytesCta;
       const uint32_t bar_leader = CG == 1 ? 0u : map_shared_to_rank(smem_addr(&s.full[stage]), 0);
-      load_stage<CG, A_MN, B_MN>(sa, sa + kABytes, tma, tmb, &s.full[stage], bar_leader, t, kb, rank);
+      load_stage<CG, A_MN, B_MN, KIND>(sa, sa + kABytes, tma, tmb, &s.full[stage], bar_leader, t, kb, rank, pol_a,
+                                       pol_b);
       issued |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -546,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx w{s.abort_flag, p.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG, STAGES, false, true, FwdSched<CG>>(s, &tmA, &tmB, p, w, rank);
+    if (lane == 0) producer_role<CG, STAGES, false, true, KIND_FWD, FwdSched<CG>>(s, &tmA, &tmB, p, w, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_role<CG, STAGES, false, true, FwdSched<CG>>(s, tmem_base, p, w);
   } else {
@@ -558,11 +594,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     using Stats = typename std::conditional<EXT, RowStatsExt, RowStats>::type;
-    Stats st{};
-    int row = 0, y = -1;
+    Stats sts[kFwdRowBlock];
+    int rows[kFwdRowBlock], ys[kFwdRowBlock];
+#pragma unroll
+    for (int q = 0; q < kFwdRowBlock; ++q) {
+      sts[q] = Stats{};
+      rows[q] = 0;
+      ys[q] = -1;
+    }
     const bool want_sum = p.want_sum_z != 0;
     while (sched.next(t)) {
       if (!epi_acquire(s, acc, acc_phase, epi_tid, w)) break;
+      // the statistics of this tile's row tile (register select, no local memory)
+      Stats st = sts[0];
+      int row = rows[0], y = ys[0];
+#pragma unroll
+      for (int q = 1; q < kFwdRowBlock; ++q)
+        if (t.sub == q) {
+          st = sts[q];
+          row = rows[q];
+          y = ys[q];
+        }
       if (t.flags & TILE_FIRST) {
         row = t.a_row + r;
         y = -1;
@@ -611,6 +663,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.part_idx != nullptr) p.part_idx[o] = st.idx;
         }
       }
+#pragma unroll
+      for (int q = 0; q < kFwdRowBlock; ++q)
+        if (t.sub == q) {
+          sts[q] = st;
+          rows[q] = row;
+          ys[q] = y;
+        }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -634,7 +693,8 @@ __device__ __forceinline__ void staging_write_row(uint8_t* box, int r, const uin
 // buffers alternate so that the copy of box i-1 overlaps the writes of box i.
 template <class WriteFn>
 __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32_t box_idx, WriteFn&& write,
-                                              const CUtensorMap* tm, int x, int y, bool reduce_add) {
+                                              const CUtensorMap* tm, int x, int y, bool reduce_add, bool hint,
+                                              uint64_t pol) {
   uint8_t* box = s.staging + (box_idx & 1u) * kStagingBytes;
   if (epi_tid == 0) bulk_wait_group_read<1>();  // the copy that last read this buffer is done
   named_barrier_sync(1, kEpiThreads);
@@ -644,6 +704,8 @@ __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32
   if (epi_tid == 0) {
     if (reduce_add)
       tma_reduce_add_2d(tm, box, x, y);
+    else if (hint)
+      tma_store_2d_hint(tm, box, x, y, pol);
     else
       tma_store_2d(tm, box, x, y);
     bulk_commit_group();
@@ -673,7 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx w{s.abort_flag, err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG, STAGES, A_MN, B_MN, WalkSched<CG, KIND>>(s, &tmA, &tmB, wp, w, rank);
+    if (lane == 0)
+      producer_role<CG, STAGES, A_MN, B_MN, KIND, WalkSched<CG, KIND>>(s, &tmA, &tmB, wp, w, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_role<CG, STAGES, A_MN, B_MN, WalkSched<CG, KIND>>(s, tmem_base, wp, w);
   } else {
@@ -685,6 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t box_idx = 0;
+    constexpr bool store_hint = OperandPolicy<KIND>::STORE != POL_NORMAL;
+    const uint64_t pol_store = make_l2_policy<OperandPolicy<KIND>::STORE>();
     while (sched.next(t)) {
       if (!epi_acquire(s, acc, acc_phase, epi_tid, w)) break;
       const uint32_t taddr = lane_addr + uint32_t(acc * kBN);
@@ -739,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           epi_store_box(
               s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
-              col0 - gp.chunk_v0, t.a_row, false);
+              col0 - gp.chunk_v0, t.a_row, false, store_hint, pol_store);
         }
       } else {
         // fp32 accumulator -> dW (store) or dX accumulator (store / add), 32 columns per box.
@@ -754,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
           epi_store_box(
               s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
-              sp.x_off + t.b_row + c, t.a_row, sp.reduce_add != 0);
+              sp.x_off + t.b_row + c, t.a_row, sp.reduce_add != 0, store_hint, pol_store);
         }
       }
       acc ^= 1;

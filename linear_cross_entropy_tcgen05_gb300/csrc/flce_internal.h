@@ -29,6 +29,15 @@ constexpr int kBarrierBytes = 256;
 // Forward split of the vocabulary: at most this many partial (max, sum-exp, sum-z)
 // triples per row.
 constexpr int kMaxSplits = 64;
+// Forward: row tiles a CTA pair computes against each W tile before moving on.
+#ifndef FLCE_FWD_ROW_BLOCK
+#define FLCE_FWD_ROW_BLOCK 4
+#endif
+constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
+// L2 cache-policy hints on the GEMMs' TMA traffic (1: on).
+#ifndef FLCE_L2_HINTS
+#define FLCE_L2_HINTS 1
+#endif
 
 // Tile walk of the non-forward GEMMs; see the kernel for how a tile index maps to
 // operand rows.

@@ -354,9 +354,18 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
   uint32_t issued = 0, last_parity = 0;
   bool ok = true;
   const bool leader = rank == 0;
+#if FLCE_WAIT_STATS
+  unsigned long long t_empty = 0;
+#endif
   while (ok && sched.next(t)) {
     for (int kb = 0; kb < t.num_kb; ++kb) {
+#if FLCE_WAIT_STATS
+      const long long c0 = clock64();
+#endif
       if (!mbar_wait(&s.empty[stage], phase ^ 1u, w)) { ok = false; break; }
+#if FLCE_WAIT_STATS
+      t_empty += (unsigned long long)(clock64() - c0);
+#endif
       if (leader) mbar_arrive_expect_tx(&s.full[stage], Geo<CG>::kTxBytes);
       uint8_t* sa = s.stage + stage * Geo<CG>::kStageBytesCta;
       const uint32_t bar_leader = CG == 1 ? 0u : map_shared_to_rank(smem_addr(&s.full[stage]), 0);
@@ -367,6 +376,9 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
   }
+#if FLCE_WAIT_STATS
+  if (leader) atomicAdd(reinterpret_cast<unsigned long long*>(w.err_word + 8 + 8 * (KIND + 1)) + 2, t_empty);
+#endif
   if (!ok) {
     if (leader) {
       // Aborting: let every copy landing on this CTA's barriers arrive before exit.
@@ -381,7 +393,7 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
   }
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, class Sched, class SP>
+template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
 __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, const SP& sp, const WaitCtx& w) {
   Sched sched(sp);
   Tile t;
@@ -391,12 +403,28 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
   uint32_t acc_phase = 0;
   bool ok = true;
   bool issued_any = false;
+#if FLCE_WAIT_STATS
+  unsigned long long t_full = 0, t_tempty = 0;
+  const long long c_start = clock64();
+#endif
   while (ok && sched.next(t)) {
+#if FLCE_WAIT_STATS
+    const long long c0 = clock64();
+#endif
     if (!mbar_wait(&s.tempty[acc], acc_phase ^ 1u, w)) { ok = false; break; }
+#if FLCE_WAIT_STATS
+    t_tempty += (unsigned long long)(clock64() - c0);
+#endif
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + uint32_t(acc * kBN);
     for (int kb = 0; kb < t.num_kb; ++kb) {
+#if FLCE_WAIT_STATS
+      const long long c1 = clock64();
+#endif
       if (!mbar_wait(&s.full[stage], phase, w)) { ok = false; break; }
+#if FLCE_WAIT_STATS
+      t_full += (unsigned long long)(clock64() - c1);
+#endif
       tc_fence_after_sync();
       const uint32_t sa = smem_addr(s.stage + stage * Geo<CG>::kStageBytesCta);
       mma_stage<CG, A_MN, B_MN>(d_tmem, sa, sa + kABytes, kb > 0);
@@ -409,6 +437,14 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
+#if FLCE_WAIT_STATS
+  {
+    unsigned long long* st = reinterpret_cast<unsigned long long*>(w.err_word + 8 + 8 * (KIND + 1));
+    atomicAdd(st + 0, t_full);
+    atomicAdd(st + 1, t_tempty);
+    atomicAdd(st + 3, (unsigned long long)(clock64() - c_start));
+  }
+#endif
   if (!ok && issued_any) {
     // Aborting: wait for the MMAs already issued before TMEM is released.
     if (CG == 1)
@@ -584,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) producer_role<CG, STAGES, false, true, KIND_FWD, FwdSched<CG>>(s, &tmA, &tmB, p, w, rank);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, STAGES, false, true, FwdSched<CG>>(s, tmem_base, p, w);
+    if (lane == 0 && rank == 0) mma_role<CG, STAGES, false, true, KIND_FWD, FwdSched<CG>>(s, tmem_base, p, w);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
@@ -738,7 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       producer_role<CG, STAGES, A_MN, B_MN, KIND, WalkSched<CG, KIND>>(s, &tmA, &tmB, wp, w, rank);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, STAGES, A_MN, B_MN, WalkSched<CG, KIND>>(s, tmem_base, wp, w);
+    if (lane == 0 && rank == 0)
+      mma_role<CG, STAGES, A_MN, B_MN, KIND, WalkSched<CG, KIND>>(s, tmem_base, wp, w);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);

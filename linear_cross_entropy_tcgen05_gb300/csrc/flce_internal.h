@@ -34,6 +34,13 @@ constexpr int kMaxSplits = 64;
 #define FLCE_FWD_ROW_BLOCK 4
 #endif
 constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
+// Diagnostic build: the GEMMs add the cycles their MMA thread waited for operands and
+// for the epilogue, its total cycles, and the cycles their producer waited for free
+// stages, to four uint64 counters at bytes 32 + 32 * (kind + 1) of the workspace header
+// (kind: -1 forward, 0 gradient, 1 dW, 2 dX) (0: off).
+#ifndef FLCE_WAIT_STATS
+#define FLCE_WAIT_STATS 0
+#endif
 // L2 cache-policy hints on the GEMMs' TMA traffic (1: on).
 #ifndef FLCE_L2_HINTS
 #define FLCE_L2_HINTS 1

@@ -201,7 +201,7 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
       break;
     }
   if (FLCE_FWD_GN > 0 && FLCE_FWD_GN <= units) gN = FLCE_FWD_GN;
-  const int64_t row_blocks = cdiv(n_tiles, kFwdRowBlock);
+  const int64_t row_blocks = cdiv(cdiv(n_tiles, kFwdRowBlock), gemm_pairs_per_cluster());  // per cluster
   if (gN > row_blocks) gN = int(row_blocks);
   int64_t S = units / gN;
   if (S > v_tiles) S = v_tiles;
@@ -428,8 +428,9 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   pp.err = err;
   FLCE_CUDA_CHECK(launch_denominator(pp, stream));  // g over every row of the batch
 
-  const int64_t d_tiles_m = cdiv(pb.D, gemm_tile_rows());  // dW rows
-  const int64_t d_tiles_n = cdiv(pb.D, kBN);               // dX columns
+  const int64_t mc = gemm_pairs_per_cluster();
+  const int64_t d_tiles_m = cdiv(cdiv(pb.D, gemm_tile_rows()), mc);  // dW row-tile groups
+  const int64_t d_tiles_n = cdiv(pb.D, kBN);                         // dX columns
   for (int64_t n0 = 0; n0 < pb.N; n0 += Nb) {
     const int64_t nb = (pb.N - n0 < Nb) ? pb.N - n0 : Nb;
     const void* Xb = static_cast<const uint8_t*>(pb.X) + size_t(n0) * size_t(pb.D) * 2;
@@ -452,7 +453,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
     pb_rows.lse = lse + n0;
     FLCE_CUDA_CHECK(launch_coef(pb_rows, int(nb), stream));
 
-    const int64_t n_tiles = cdiv(nb, gemm_tile_rows());
+    const int64_t n_tiles = cdiv(cdiv(nb, gemm_tile_rows()), mc);  // row-tile groups
     for (int64_t v0 = 0, band_i = 0; v0 < pb.V; v0 += Vc, ++band_i) {
       const int64_t vc = (pb.V - v0 < Vc) ? pb.V - v0 : Vc;
       const int64_t vt = cdiv(vc, kBN);

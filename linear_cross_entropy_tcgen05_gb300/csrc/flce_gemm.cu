@@ -72,18 +72,25 @@ struct Tile {
   int flags;
 };
 
+// A cluster is MC CTA pairs (CG = 2 CTAs each). The pairs of a cluster compute tiles
+// that share their B operand: pair 0 loads it once and multicasts it to the other pairs.
 struct Pair {
-  int cid;        // cluster (CTA pair) index
+  int cid;        // cluster index
   int nclusters;  // clusters in the grid
-  int rank;       // 0 = leader, 1 = peer (always 0 for CG = 1)
+  int pair;       // pair within the cluster
+  int rank;       // CTA within the pair: 0 = leader (issues the MMAs), 1 = peer
+  int leader;     // %cluster_ctarank of this pair's leader
 };
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ Pair pair_id() {
   Pair p;
-  p.cid = int(blockIdx.x) / CG;
-  p.nclusters = int(gridDim.x) / CG;
-  p.rank = CG == 1 ? 0 : int(cluster_ctarank());
+  p.cid = int(blockIdx.x) / (CG * MC);
+  p.nclusters = int(gridDim.x) / (CG * MC);
+  const int cta = (CG * MC == 1) ? 0 : int(cluster_ctarank());
+  p.pair = cta / CG;
+  p.rank = cta % CG;
+  p.leader = cta - p.rank;
   return p;
 }
 
@@ -99,18 +106,19 @@ __device__ __forceinline__ Pair pair_id() {
 // is streamed from HBM once per row block and re-read from L2 right away. Running
 // statistics stay in registers (one set per row tile of the block) and are written once
 // per (row, range).
-template <int CG>
+template <int CG, int MC>
 struct FwdSched {
   int n_tiles, v_tiles, gN, S, num_kb;
-  int n_off, split, rank;
+  int n_off, split, rank, pair;
   int g, vt, vt0, vt_end, range, rb0, rb_tiles, j;
 
   __device__ explicit FwdSched(const FwdParams& p) : n_tiles(p.n_tiles), v_tiles(p.v_tiles), gN(p.gN), S(p.S),
                                                      num_kb(p.num_kb) {
-    const Pair pr = pair_id<CG>();
+    const Pair pr = pair_id<CG, MC>();
     n_off = pr.cid % gN;
     split = pr.cid / gN;
     rank = pr.rank;
+    pair = pr.pair;
     g = -1;
     vt = vt0 = vt_end = range = rb0 = rb_tiles = j = 0;
   }
@@ -118,9 +126,12 @@ struct FwdSched {
   __device__ bool next(Tile& t) {
     if (vt >= vt_end) {
       ++g;
-      rb0 = (g * gN + n_off) * kFwdRowBlock;
-      if (rb0 >= n_tiles) return false;
-      rb_tiles = n_tiles - rb0 < kFwdRowBlock ? n_tiles - rb0 : kFwdRowBlock;
+      // the cluster's MC row blocks; the pairs walk in lockstep, so a pair whose block
+      // runs past the last row tile computes zero rows (loads beyond N read zeros)
+      const int cluster_rb0 = (g * gN + n_off) * MC * kFwdRowBlock;
+      if (cluster_rb0 >= n_tiles) return false;
+      rb0 = cluster_rb0 + pair * kFwdRowBlock;
+      rb_tiles = (MC > 1 || n_tiles - rb0 >= kFwdRowBlock) ? kFwdRowBlock : n_tiles - rb0;
       range = (split + g) % S;
       vt0 = vt = int((long long)range * v_tiles / S);
       vt_end = int((long long)(range + 1) * v_tiles / S);
@@ -148,21 +159,24 @@ struct FwdSched {
 //   WALK_DW  : major = 256-column vocabulary tile, minor = row tile of D.
 //   WALK_DX  : major = row tile of the band, minor = 256-column tile of D.
 // Row tiles are kBM * CG rows (this CTA takes rows rank*128 .. rank*128+127 of each).
-template <int CG, int KIND>
+// With MC pairs per cluster the row-tile index counts groups of MC row tiles (one per
+// pair, all with the same B); the host sizes the walk in those units.
+template <int CG, int MC, int KIND>
 struct WalkSched {
   WalkParams w;
-  int i, step, rank;
+  int i, step, rank, pair;
   __device__ explicit WalkSched(const WalkParams& p) : w(p) {
-    const Pair pr = pair_id<CG>();
+    const Pair pr = pair_id<CG, MC>();
     i = pr.cid;
     step = pr.nclusters;
     rank = pr.rank;
+    pair = pr.pair;
   }
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;
     const int major = i / w.tiles_minor;
     const int minor = i - major * w.tiles_minor;
-    const int rows = (KIND == WALK_DW) ? minor : major;
+    const int rows = ((KIND == WALK_DW) ? minor : major) * MC + pair;
     const int cols = (KIND == WALK_DW) ? major : minor;
     t.a_row = rows * Geo<CG>::kTileRows + rank * kBM;
     t.b_row = w.b_row_off + cols * kBN;
@@ -215,11 +229,11 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
   return s;
 }
 
-template <int CG, int STAGES>
+template <int CG, int MC, int STAGES>
 __device__ __forceinline__ void init_barriers(const Smem& s) {
   for (int i = 0; i < STAGES; ++i) {
     mbar_init(&s.full[i], 1);
-    mbar_init(&s.empty[i], 1);
+    mbar_init(&s.empty[i], MC);  // one commit from each pair's MMA (B is shared)
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(&s.tfull[i], 1);
@@ -232,7 +246,7 @@ __device__ __forceinline__ void init_barriers(const Smem& s) {
   fence_barrier_init();
 }
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void tmem_setup(const Smem& s, int warp) {
   if (warp == 1) {
     if (CG == 1) {
@@ -245,15 +259,15 @@ __device__ __forceinline__ void tmem_setup(const Smem& s, int warp) {
   }
   tc_fence_before_sync();
   __syncthreads();
-  if (CG == 2) cluster_sync_all();  // barriers initialised and TMEM allocated in both CTAs
+  if (CG * MC > 1) cluster_sync_all();  // barriers initialised and TMEM allocated in every CTA
   tc_fence_after_sync();
 }
 
-template <int CG>
+template <int CG, int MC>
 __device__ __forceinline__ void tmem_teardown(uint32_t tmem_base, int warp) {
   tc_fence_before_sync();
   __syncthreads();
-  if (CG == 2) cluster_sync_all();  // no peer still signals this CTA's barriers or reads its TMEM
+  if (CG * MC > 1) cluster_sync_all();  // no other CTA still signals this CTA's barriers
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
@@ -280,10 +294,10 @@ struct OperandPolicy<KIND_FWD> {
   static constexpr int STORE = POL_NORMAL;
 };
 
-template <int CG, bool A_MN, bool B_MN, int KIND>
+template <int CG, int MC, bool A_MN, bool B_MN, int KIND>
 __device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUtensorMap* tma, const CUtensorMap* tmb,
                                            uint64_t* bar_local, uint32_t bar_leader, const Tile& t, int kb,
-                                           int rank, uint64_t pol_a, uint64_t pol_b) {
+                                           int rank, int pair, uint64_t pol_a, uint64_t pol_b) {
   const int ka = t.a_k0 + kb * kBK;
   const int kbb = t.b_k0 + kb * kBK;
   const int b0 = t.b_row + rank * Geo<CG>::kBRows;
@@ -308,12 +322,25 @@ __device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUten
 #pragma unroll
     for (int j = 0; j < kBM / 64; ++j) load(sa + j * 8192, tma, t.a_row + 64 * j, ka, ha, pol_a);  // {64 M, 64 K}
   }
-  if (!B_MN) {
-    load(sb, tmb, kbb, b0, hb, pol_b);  // box {64 K, 256/CG rows}
-  } else {
+  if (MC == 1) {
+    if (!B_MN) {
+      load(sb, tmb, kbb, b0, hb, pol_b);  // box {64 K, 256/CG rows}
+    } else {
 #pragma unroll
-    for (int j = 0; j < Geo<CG>::kBRows / 64; ++j)
-      load(sb + j * 8192, tmb, b0 + 64 * j, kbb, hb, pol_b);  // {64 N, 64 K}
+      for (int j = 0; j < Geo<CG>::kBRows / 64; ++j)
+        load(sb + j * 8192, tmb, b0 + 64 * j, kbb, hb, pol_b);  // {64 N, 64 K}
+    }
+  } else if (pair == 0) {
+    // this CTA's half of B goes to the same-rank CTA of every pair; each copy completes on
+    // its destination pair's leader barrier (the barrier operand names this pair's leader)
+    const uint16_t mask = uint16_t(((1u << (CG * MC)) - 1u) & (0x5555u << rank));
+    if (!B_MN) {
+      tma_load_2d_pair_mc(sb, tmb, bar_leader, kbb, b0, mask, hb, pol_b);
+    } else {
+#pragma unroll
+      for (int j = 0; j < Geo<CG>::kBRows / 64; ++j)
+        tma_load_2d_pair_mc(sb + j * 8192, tmb, bar_leader, b0 + 64 * j, kbb, mask, hb, pol_b);
+    }
   }
 }
 
@@ -334,17 +361,28 @@ __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sa, uint32_t
   }
 }
 
-template <int CG>
-__device__ __forceinline__ void commit_both(uint64_t* bar) {
+// Stage release: every CTA of the cluster (pair 0 also loaded B for the other pairs).
+template <int CG, int MC>
+__device__ __forceinline__ void commit_stage(uint64_t* bar) {
   if (CG == 1)
     tc_commit(bar);
   else
-    tc_commit_pair_multicast(bar, uint16_t(0x3));
+    tc_commit_pair_multicast(bar, uint16_t((1u << (CG * MC)) - 1u));
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
+// Accumulator ready: the two CTAs of this pair.
+template <int CG>
+__device__ __forceinline__ void commit_pair(uint64_t* bar, int leader) {
+  if (CG == 1)
+    tc_commit(bar);
+  else
+    tc_commit_pair_multicast(bar, uint16_t(0x3u << leader));
+}
+
+template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
 __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* tma, const CUtensorMap* tmb,
-                                              const SP& sp, const WaitCtx& w, int rank) {
+                                              const SP& sp, const WaitCtx& w, const Pair& pr) {
+  const int rank = pr.rank;
   Sched sched(sp);
   const uint64_t pol_a = make_l2_policy<OperandPolicy<KIND>::A>();
   const uint64_t pol_b = make_l2_policy<OperandPolicy<KIND>::B>();
@@ -368,9 +406,10 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
 #endif
       if (leader) mbar_arrive_expect_tx(&s.full[stage], Geo<CG>::kTxBytes);
       uint8_t* sa = s.stage + stage * Geo<CG>::kStageBytesCta;
-      const uint32_t bar_leader = CG == 1 ? 0u : map_shared_to_rank(smem_addr(&s.full[stage]), 0);
-      load_stage<CG, A_MN, B_MN, KIND>(sa, sa + kABytes, tma, tmb, &s.full[stage], bar_leader, t, kb, rank, pol_a,
-                                       pol_b);
+      const uint32_t bar_leader =
+          CG == 1 ? 0u : map_shared_to_rank(smem_addr(&s.full[stage]), uint32_t(pr.leader));
+      load_stage<CG, MC, A_MN, B_MN, KIND>(sa, sa + kABytes, tma, tmb, &s.full[stage], bar_leader, t, kb, rank,
+                                           pr.pair, pol_a, pol_b);
       issued |= 1u << stage;
       last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -393,8 +432,9 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
   }
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
-__device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, const SP& sp, const WaitCtx& w) {
+template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
+__device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, const SP& sp, const WaitCtx& w,
+                                         int leader) {
   Sched sched(sp);
   Tile t;
   int stage = 0;
@@ -429,11 +469,11 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
       const uint32_t sa = smem_addr(s.stage + stage * Geo<CG>::kStageBytesCta);
       mma_stage<CG, A_MN, B_MN>(d_tmem, sa, sa + kABytes, kb > 0);
       issued_any = true;
-      commit_both<CG>(&s.empty[stage]);
+      commit_stage<CG, MC>(&s.empty[stage]);
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    commit_both<CG>(&s.tfull[acc]);
+    commit_pair<CG>(&s.tfull[acc], leader);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -472,13 +512,13 @@ __device__ __forceinline__ bool epi_acquire(const Smem& s, int acc, uint32_t acc
 
 // This thread has finished reading accumulator `acc` (all its tcgen05.ld waited on).
 template <int CG>
-__device__ __forceinline__ void epi_release(const Smem& s, int acc) {
+__device__ __forceinline__ void epi_release(const Smem& s, int acc, int leader) {
   tc_fence_before_sync();
   if (CG == 1) {
     mbar_arrive(&s.tempty[acc]);
   } else {
     __syncwarp();
-    if (lane_id() == 0) mbar_arrive_cluster(map_shared_to_rank(smem_addr(&s.tempty[acc]), 0));
+    if (lane_id() == 0) mbar_arrive_cluster(map_shared_to_rank(smem_addr(&s.tempty[acc]), uint32_t(leader)));
   }
 }
 
@@ -598,7 +638,7 @@ __device__ __forceinline__ void online_update_ext(RowStatsExt& st, const uint32_
   }
 }
 
-template <int CG, int STAGES, bool EXT>
+template <int CG, int MC, int STAGES, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_forward_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const FwdParams p) {
@@ -606,26 +646,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem s = carve_smem<CG, STAGES, 0>(smem_raw);
   const int warp = int(threadIdx.x) >> 5;
   const uint32_t lane = lane_id();
-  const int rank = pair_id<CG>().rank;
+  const Pair pr = pair_id<CG, MC>();
+  const int rank = pr.rank;
 
-  if (threadIdx.x == 0) init_barriers<CG, STAGES>(s);
+  if (threadIdx.x == 0) init_barriers<CG, MC, STAGES>(s);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  tmem_setup<CG>(s, warp);
+  tmem_setup<CG, MC>(s, warp);
   const uint32_t tmem_base = *s.tmem_slot;
   const WaitCtx w{s.abort_flag, p.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG, STAGES, false, true, KIND_FWD, FwdSched<CG>>(s, &tmA, &tmB, p, w, rank);
+    if (lane == 0) producer_role<CG, MC, STAGES, false, true, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, p, w, pr);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, STAGES, false, true, KIND_FWD, FwdSched<CG>>(s, tmem_base, p, w);
+    if (lane == 0 && rank == 0)
+      mma_role<CG, MC, STAGES, false, true, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
     const uint32_t lane_addr = tmem_base + (uint32_t(32 * (warp & 3)) << 16);
-    FwdSched<CG> sched(p);
+    FwdSched<CG, MC> sched(p);
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -669,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(taddr + uint32_t(c), r0);
         tmem_ld_32cols(taddr + uint32_t(c + 32), r1);
         tc_wait_ld();
-        if (c + 64 == kBN) epi_release<CG>(s, acc);
+        if (c + 64 == kBN) epi_release<CG>(s, acc, pr.leader);
         const int col0 = t.b_row + c;
         if constexpr (EXT) {
           if (!tail_tile) {
@@ -710,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  tmem_teardown<CG>(tmem_base, warp);
+  tmem_teardown<CG, MC>(tmem_base, warp);
 }
 
 // ---------------------------------------------------------------------------------
@@ -748,7 +790,7 @@ __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32
   }
 }
 
-template <int CG, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI, bool EXT>
+template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_walk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const WalkParams wp, const GradEpiParams gp,
@@ -757,30 +799,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Smem s = carve_smem<CG, STAGES, 2>(smem_raw);
   const int warp = int(threadIdx.x) >> 5;
   const uint32_t lane = lane_id();
-  const int rank = pair_id<CG>().rank;
+  const Pair pr = pair_id<CG, MC>();
+  const int rank = pr.rank;
   int* err = (EPI == 0) ? gp.err : sp.err;
 
-  if (threadIdx.x == 0) init_barriers<CG, STAGES>(s);
+  if (threadIdx.x == 0) init_barriers<CG, MC, STAGES>(s);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
   }
-  tmem_setup<CG>(s, warp);
+  tmem_setup<CG, MC>(s, warp);
   const uint32_t tmem_base = *s.tmem_slot;
   const WaitCtx w{s.abort_flag, err};
 
   if (warp == 0) {
     if (lane == 0)
-      producer_role<CG, STAGES, A_MN, B_MN, KIND, WalkSched<CG, KIND>>(s, &tmA, &tmB, wp, w, rank);
+      producer_role<CG, MC, STAGES, A_MN, B_MN, KIND, WalkSched<CG, MC, KIND>>(s, &tmA, &tmB, wp, w, pr);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role<CG, STAGES, A_MN, B_MN, KIND, WalkSched<CG, KIND>>(s, tmem_base, wp, w);
+      mma_role<CG, MC, STAGES, A_MN, B_MN, KIND, WalkSched<CG, MC, KIND>>(s, tmem_base, wp, w, pr.leader);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);
     const uint32_t lane_addr = tmem_base + (uint32_t(32 * (warp & 3)) << 16);
-    WalkSched<CG, KIND> sched(wp);
+    WalkSched<CG, MC, KIND> sched(wp);
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -804,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(taddr + uint32_t(c), r0);
           tmem_ld_32cols(taddr + uint32_t(c + 32), r1);
           tc_wait_ld();
-          if (c + 64 == kBN) epi_release<CG>(s, acc);
+          if (c + 64 == kBN) epi_release<CG>(s, acc, pr.leader);
           const int col0 = t.b_row + c;  // global vocabulary column
           uint4 chunks[8];
           uint32_t* packed = reinterpret_cast<uint32_t*>(chunks);
@@ -850,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r0[32];
           tmem_ld_32cols(taddr + uint32_t(c), r0);
           tc_wait_ld();
-          if (c + 32 == kBN) epi_release<CG>(s, acc);
+          if (c + 32 == kBN) epi_release<CG>(s, acc, pr.leader);
           uint4 chunks[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
@@ -864,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (epi_tid == 0) bulk_wait_group<0>();  // every store has landed before the CTA exits
   }
-  tmem_teardown<CG>(tmem_base, warp);
+  tmem_teardown<CG, MC>(tmem_base, warp);
 }
 
 // ---------------------------------------------------------------------------------
@@ -873,6 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace {
 
 constexpr int kCG = 2;           // CTA pair (cta_group::2) for every GEMM
+constexpr int kMC = FLCE_PAIRS_PER_CLUSTER;  // pairs sharing B through TMA multicast
 constexpr int kFwdStages = 7;    // 7 x 32 KB
 constexpr int kWalkStages = 6;   // 6 x 32 KB + 2 x 16 KB epilogue boxes
 
@@ -888,7 +932,7 @@ cudaLaunchConfig_t make_config(int grid, size_t smem, cudaStream_t stream, cudaL
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCG;
+  attr[0].val.clusterDim.x = kCG * kMC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -907,22 +951,22 @@ int max_clusters(Kern kernel, size_t smem, int slot) {
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(sms - sms % kCG, smem, nullptr, attr);
+  cudaLaunchConfig_t cfg = make_config(sms - sms % (kCG * kMC), smem, nullptr, attr);
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    n = sms / kCG;
+    n = sms / (kCG * kMC);
   }
   cache[dev][slot] = n;
   return n;
 }
 
 template <bool EXT>
-auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kFwdStages, EXT>; }
+auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, EXT>; }
 template <bool EXT>
-auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, true, WALK_GRAD, 0, EXT>; }
-auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, true, true, WALK_DW, 1, false>; }
-auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kWalkStages, false, false, WALK_DX, 1, false>; }
+auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, true, WALK_GRAD, 0, EXT>; }
+auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, WALK_DW, 1, false>; }
+auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, false, WALK_DX, 1, false>; }
 
 constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
 constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
@@ -938,13 +982,15 @@ cudaError_t launch_walk(Kern kernel, const CUtensorMap& tmA, const CUtensorMap& 
   if (maxc <= 0) return cudaErrorInvalidConfiguration;
   const int clusters = w.total_tiles < maxc ? w.total_tiles : maxc;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(clusters * kCG, kWalkSmem, stream, attr);
+  cudaLaunchConfig_t cfg = make_config(clusters * kCG * kMC, kWalkSmem, stream, attr);
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, w, g, s);
 }
 
 }  // namespace
 
 int gemm_tile_rows() { return kBM * kCG; }
+
+int gemm_pairs_per_cluster() { return kMC; }
 
 int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
 
@@ -957,7 +1003,7 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(p.gN * p.S * kCG, kFwdSmem, stream, attr);
+  cudaLaunchConfig_t cfg = make_config(p.gN * p.S * kCG * kMC, kFwdSmem, stream, attr);
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 

@@ -41,6 +41,11 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_WAIT_STATS
 #define FLCE_WAIT_STATS 0
 #endif
+// CTA pairs per cluster: 2 makes two pairs share every B tile (one TMA multicast load
+// instead of two), 1 gives every pair its own loads.
+#ifndef FLCE_PAIRS_PER_CLUSTER
+#define FLCE_PAIRS_PER_CLUSTER 2
+#endif
 // L2 cache-policy hints on the GEMMs' TMA traffic (1: on).
 #ifndef FLCE_L2_HINTS
 #define FLCE_L2_HINTS 1
@@ -160,6 +165,8 @@ struct ColsumParams {
 
 // Rows of one GEMM output tile (a CTA pair: 2 x 128).
 int gemm_tile_rows();
+// CTA pairs per cluster (pairs of a cluster share B); walks count row tiles in these units.
+int gemm_pairs_per_cluster();
 // Rows (K-major) or columns (MN-major) of the B operand each CTA loads: 256 / pair size.
 int gemm_b_rows_per_cta();
 // CTA pairs of the forward GEMM that can be resident at once on the current device.

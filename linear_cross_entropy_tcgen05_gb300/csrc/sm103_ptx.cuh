@@ -363,3 +363,28 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const 
 }
 
 }  // namespace flce
+
+namespace flce {
+
+// Global -> shared memory of every CTA in `cta_mask` (same offset in each), for pair
+// MMAs: each destination CTA's copy completes on the barrier of that CTA's pair leader,
+// at the offset of `bar_cluster_addr` (which names the issuing pair's leader).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr,
+                                                    int x, int y, uint16_t cta_mask, bool hint, uint64_t pol) {
+  if (hint)
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y),
+        "h"(cta_mask), "l"(pol)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(x), "r"(y),
+        "h"(cta_mask)
+        : "memory");
+}
+
+}  // namespace flce

@@ -139,9 +139,9 @@ def barrier(world: int):
 def kernel_launches_per_step(N, D, V, reduction):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
     backward denominator + row coefficients + 3 GEMMs per vocabulary band + the dX cast."""
-    kBN = 256
-    vc = max(kBN, min(16384, ((1 << 30) // (2 * N)) // kBN * kBN))
-    half = (((V + 1) // 2) + kBN - 1) // kBN * kBN
+    unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
+    vc = max(unit, min(16384, ((1 << 30) // (2 * N)) // unit * unit))
+    half = (((V + 1) // 2) + unit - 1) // unit * unit
     vc = min(vc, half)
     bands = -(-V // vc)
     fwd = 1 + 1 + (0 if reduction == "none" else 1)

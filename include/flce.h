@@ -141,6 +141,12 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
  *   dZ = dU (1 - (u/softcap)^2) with a softcap,  dbias = sum_i dZ_i,
  *   predicted_i = argmax_j u_ij (smallest index on ties), accuracy = matches / valid rows.
  * Zero-initialise the struct and set what you need; NULL means "no options". */
+/* Storage of W and dW. FLCE_WEIGHT_DV: W [D, V] and dW [D, V], row-major (the default,
+ * the layout of "Cutting LLM Memory by 84%", "The Logit Bottleneck"). FLCE_WEIGHT_VD:
+ * W [V, D] and dW [V, D], row-major -- the weight of an nn.Linear(D, V) language-model
+ * head, taken as it is stored (no transposed copy). Not a part of the pages' method. */
+typedef enum { FLCE_WEIGHT_DV = 0, FLCE_WEIGHT_VD = 1 } flce_weight_layout;
+
 typedef struct flce_options {
   float softcap;             /* > 0: cap the logits with softcap*tanh(z/softcap); 0: off */
   const float* bias;         /* device fp32 [V] added to every row's logits, or NULL */
@@ -155,6 +161,7 @@ typedef struct flce_options {
                                 Production": micro-batching along N), so the workspace is
                                 flce_workspace_size(row_band, D, V, 1) whatever N is; dW then
                                 accumulates across bands (fp32 adds in a fixed order). 0: all rows. */
+  int32_t weight_layout;     /* flce_weight_layout of W and dW (FLCE_WEIGHT_DV if 0) */
 } flce_options;
 
 /* flce_forward with options (NULL behaves exactly like flce_forward). Vocabulary
@@ -214,6 +221,14 @@ const char* flce_status_string(flce_status status);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int flce_version(void);
+
+/* Which call failed the last time an entry point returned FLCE_ERR_CUDA on the calling
+ * thread: the CUDA runtime or driver call and its error name, e.g.
+ * "cudaMemsetAsync(...): cudaErrorInvalidValue". Empty if that never happened on this
+ * thread; later successful calls do not clear it. The string is thread-local, owned by
+ * the library and valid until the thread's next library call. Diagnostics only: the
+ * pages have no counterpart. */
+const char* flce_last_error_detail(void);
 
 /* Forward pass without a workspace, for callers that cannot allocate device memory
  * (code inside an allocator or memory-pool callback, runtimes that give a fixed

@@ -7,7 +7,9 @@ marshal torch tensors into pointers and sizes and call the library; every step o
 the computation runs in the library's CUDA kernels. There is no CPU fallback: if
 the library is missing, ``load_library`` raises.
 
-``linear_cross_entropy`` wraps the two calls in a ``torch.autograd.Function``.
+``linear_cross_entropy`` wraps the two calls in a ``torch.autograd.Function``. W is
+[D, V] by default; ``weight_layout="vd"`` takes the [V, D] weight of an
+``nn.Linear(D, V, bias=False)`` language-model head as it is (dW then has that layout too).
 """
 from __future__ import annotations
 
@@ -21,13 +23,14 @@ __all__ = [
     "flce_check_device_error", "flce_status_string", "flce_version", "linear_cross_entropy",
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
-    "flce_combine_shards",
+    "flce_combine_shards", "WEIGHT_LAYOUTS", "flce_last_error_detail",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
+WEIGHT_LAYOUTS = {"dv": 0, "vd": 1}  # flce_weight_layout: W [D, V] or W [V, D]
 STATUS = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_ALIGNMENT", 3: "FLCE_ERR_UNSUPPORTED_DEVICE",
     4: "FLCE_ERR_WORKSPACE_TOO_SMALL", 5: "FLCE_ERR_REDUCTION_NONE_GRAD", 6: "FLCE_ERR_CUDA",
@@ -35,7 +38,8 @@ STATUS = {
 }
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
-                    "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards")
+                    "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards",
+                    "flce_last_error_detail")
 
 
 class FlceOptions(ctypes.Structure):
@@ -44,21 +48,32 @@ class FlceOptions(ctypes.Structure):
     _fields_ = [("softcap", ctypes.c_float), ("bias", ctypes.c_void_p), ("class_weight", ctypes.c_void_p),
                 ("predicted", ctypes.c_void_p), ("accuracy", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
                 ("dX_f32", ctypes.c_void_p), ("v_offset", ctypes.c_int64), ("v_total", ctypes.c_int64),
-                ("row_band", ctypes.c_int64)]
+                ("row_band", ctypes.c_int64), ("weight_layout", ctypes.c_int32)]
+
+
+def _layout(weight_layout) -> int:
+    return WEIGHT_LAYOUTS[weight_layout] if isinstance(weight_layout, str) else int(weight_layout)
 
 
 def make_options(softcap: float = 0.0, bias=None, class_weight=None, predicted=None, accuracy=None, dbias=None,
-                 dX_f32=None, v_offset: int = 0, v_total: int = 0, row_band: int = 0):
+                 dX_f32=None, v_offset: int = 0, v_total: int = 0, row_band: int = 0, weight_layout="dv"):
     """An ``flce_options`` value (device tensors become pointers)."""
     return FlceOptions(float(softcap), _ptr(bias), _ptr(class_weight), _ptr(predicted), _ptr(accuracy),
-                       _ptr(dbias), _ptr(dX_f32), int(v_offset), int(v_total), int(row_band))
+                       _ptr(dbias), _ptr(dX_f32), int(v_offset), int(v_total), int(row_band),
+                       _layout(weight_layout))
+
+
+def _vocab(W, options) -> int:
+    """V from W's shape: [D, V], or [V, D] when the options say so."""
+    return W.shape[0] if options is not None and options.weight_layout == 1 else W.shape[1]
 
 
 class FLCEError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         self.name = STATUS.get(status, f"status {status}")
-        super().__init__(f"{where}: {flce_status_string(status)}")
+        detail = f" ({flce_last_error_detail()})" if status == 6 else ""
+        super().__init__(f"{where}: {flce_status_string(status)}{detail}")
 
 
 def library_path() -> str:
@@ -88,6 +103,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_version.argtypes = []
     lib.flce_version.restype = ctypes.c_int
+    lib.flce_last_error_detail.argtypes = []
+    lib.flce_last_error_detail.restype = ctypes.c_char_p
     op = ctypes.POINTER(FlceOptions)
     lib.flce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp, sz, vp]
     lib.flce_forward_ex.restype = ctypes.c_int
@@ -112,6 +129,11 @@ def flce_status_string(status: int) -> str:
 
 def flce_version() -> int:
     return int(load_library().flce_version())
+
+
+def flce_last_error_detail() -> str:
+    """The CUDA call behind the calling thread's last FLCE_ERR_CUDA ('' if none)."""
+    return load_library().flce_last_error_detail().decode()
 
 
 def flce_workspace_size(N: int, D: int, V: int, for_backward: bool) -> int:
@@ -192,7 +214,7 @@ def flce_forward_ex(X, W, targets, loss, lse, workspace, ignore_index: int = -10
                     stream=None, raise_on_error: bool = True) -> int:
     """Call flce_forward_ex (``options`` from ``make_options``)."""
     st = load_library().flce_forward_ex(
-        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(loss), _ptr(lse),
         _ptr(workspace), _nbytes(workspace), _stream(stream))
     if raise_on_error:
@@ -205,7 +227,7 @@ def flce_backward_ex(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_ind
                      options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
     """Call flce_backward_ex (dX may be None when options.dX_f32 is set)."""
     st = load_library().flce_backward_ex(
-        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(dX),
         _ptr(dW), _ptr(workspace), _nbytes(workspace), _stream(stream))
     if raise_on_error:
@@ -218,7 +240,7 @@ def flce_forward_backward(X, W, targets, grad_out, loss, lse, dX, dW, workspace,
                           options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
     """Call flce_forward_backward (workspace: flce_workspace_size(N, D, V, 2) bytes)."""
     st = load_library().flce_forward_backward(
-        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], W.shape[1], int(ignore_index),
+        _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(loss),
         _ptr(lse), _ptr(dX), _ptr(dW), _ptr(workspace), _nbytes(workspace), _stream(stream))
     if raise_on_error:
@@ -262,13 +284,15 @@ def _workspace(N, D, V, device, for_backward, cache=None):
     return torch.empty(max(need, 16), dtype=torch.uint8, device=device)
 
 
-def _validate(X, W, targets):
+def _validate(X, W, targets, layout=0):
     if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError("X and W must be bfloat16")
     if targets.dtype != torch.int32:
         raise TypeError("targets must be int32")
-    if X.dim() != 2 or W.dim() != 2 or targets.dim() != 1 or X.shape[1] != W.shape[0] or X.shape[0] != targets.shape[0]:
-        raise ValueError("expected X [N,D], W [D,V], targets [N]")
+    wd = W.shape[1] if layout == 1 else W.shape[0]
+    if X.dim() != 2 or W.dim() != 2 or targets.dim() != 1 or X.shape[1] != wd or X.shape[0] != targets.shape[0]:
+        raise ValueError(("expected X [N,D], W [V,D]" if layout == 1 else "expected X [N,D], W [D,V]")
+                         + ", targets [N]")
     if not (X.is_cuda and W.is_cuda and targets.is_cuda):
         raise ValueError("X, W and targets must be CUDA tensors")
     if not (X.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
@@ -280,47 +304,50 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, X, W, targets, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",
-                softcap=0.0, bias=None, class_weight=None):
-        _validate(X, W, targets)
+                softcap=0.0, bias=None, class_weight=None, weight_layout="dv"):
+        layout = _layout(weight_layout)
+        _validate(X, W, targets, layout)
         N, D = X.shape
-        V = W.shape[1]
+        V = W.shape[0] if layout == 1 else W.shape[1]
         ws = _workspace(N, D, V, X.device, False)
         loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
         lse = torch.empty(N, dtype=torch.float32, device=X.device)
         b32 = bias.detach().float().contiguous() if bias is not None else None
         w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32)
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout)
         flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction, opts)
         ctx.save_for_backward(X, W, targets, lse)
         ctx.extra = (b32, w32, bias is not None and bias.requires_grad, bias.dtype if bias is not None else None)
-        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction, softcap)
+        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout)
         return loss if reduction == "none" else loss[0]
 
     @staticmethod
     def backward(ctx, grad_loss):
         X, W, targets, lse = ctx.saved_tensors
         b32, w32, want_db, b_dtype = ctx.extra
-        ignore_index, label_smoothing, zloss_scale, reduction, softcap = ctx.opts
+        ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout = ctx.opts
         if reduction == "none":
             raise RuntimeError("reduction='none' has no fused backward (FLCE_ERR_REDUCTION_NONE_GRAD)")
         N, D = X.shape
-        V = W.shape[1]
+        V = W.shape[0] if layout == 1 else W.shape[1]
         ws = _workspace(N, D, V, X.device, True)
         g = grad_loss.detach().to(device=X.device, dtype=torch.float32).reshape(1).contiguous()
         dX = torch.empty_like(X)
-        dW = torch.empty(D, V, dtype=torch.float32, device=X.device)
+        dW = torch.empty(W.shape, dtype=torch.float32, device=X.device)
         db = torch.empty(V, dtype=torch.float32, device=X.device) if want_db else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db)
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db, weight_layout=layout)
         flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction,
                          opts)
         return (dX, dW.to(W.dtype), None, None, None, None, None, None,
-                db.to(b_dtype) if db is not None else None, None)
+                db.to(b_dtype) if db is not None else None, None, None)
 
 
 def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,
                          zloss_scale: float = 0.0, reduction: str = "mean", softcap: float = 0.0, bias=None,
-                         class_weight=None):
+                         class_weight=None, weight_layout: str = "dv"):
     """Fused linear cross-entropy of X [N,D] (bf16), W [D,V] (bf16), int32 targets [N].
+
+    ``weight_layout="vd"`` takes W as [V,D] (an ``nn.Linear(D, V)`` weight) instead.
 
     Optional: a logit ``softcap``, a ``bias`` [V] (its gradient is returned through
     autograd) and per-class weights ``class_weight`` [V]. The gradient of W is
@@ -328,4 +355,4 @@ def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothin
     ``flce_backward`` directly to keep the fp32 dW.
     """
     return LinearCrossEntropyFunction.apply(X, W, targets, ignore_index, label_smoothing, zloss_scale, reduction,
-                                            softcap, bias, class_weight)
+                                            softcap, bias, class_weight, weight_layout)

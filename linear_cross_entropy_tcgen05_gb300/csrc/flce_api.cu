@@ -15,6 +15,7 @@
 //        dX GEMM       : dX_acc (+)= G W[:, band]^T (fp32, TMA element-wise add);
 //   3. cast dX_acc to bf16.
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -81,21 +82,23 @@ struct BwdLayout {
   int64_t Vc;
 };
 
-// Width of the gradient band: as many 256-column tiles as fit in the byte budget, at
-// most kMaxBandCols (wider bands measured no faster and cost memory), and never more
-// than half the vocabulary (rounded up to a tile), so that no buffer holds N x V values
-// once V exceeds one tile.
+// Width of the gradient band: a multiple of one cluster's vocabulary tiles (2 pairs x 256
+// rows when dW is [V, D], so no tile of a band reaches into the next), as many as fit in
+// the byte budget, at most kMaxBandCols (wider bands measured no faster and cost memory),
+// and never more than half the vocabulary (rounded up to that unit), so that no buffer
+// holds N x V values once V exceeds one unit.
 constexpr int64_t kMaxBandCols = 16384;
 
 int64_t band_width(int64_t N, int64_t D, int64_t V) {
-  int64_t vc = (kGradBandBudget / (2 * N)) / kBN * kBN;
+  const int64_t unit = int64_t(gemm_tile_rows()) * gemm_pairs_per_cluster();
+  int64_t vc = (kGradBandBudget / (2 * N)) / unit * unit;
   if (vc > kMaxBandCols) vc = kMaxBandCols;
   if (FLCE_BAND_W_L2_BYTES > 0) {
-    const int64_t l2 = (FLCE_BAND_W_L2_BYTES / (2 * D)) / kBN * kBN;
+    const int64_t l2 = (FLCE_BAND_W_L2_BYTES / (2 * D)) / unit * unit;
     if (l2 < vc) vc = l2;
   }
-  if (vc < kBN) vc = kBN;
-  const int64_t half = cdiv(cdiv(V, 2), kBN) * kBN;
+  if (vc < unit) vc = unit;
+  const int64_t half = cdiv(cdiv(V, 2), unit) * unit;
   if (vc > half) vc = half;
   return vc;
 }
@@ -121,9 +124,29 @@ bool sizes_in_range(int64_t N, int64_t D, int64_t V) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// --- the detail behind FLCE_ERR_CUDA (per calling thread) ---------------------------
+thread_local char g_detail[192];
+
+void note_error(const char* what, const char* why) {
+  std::snprintf(g_detail, sizeof(g_detail), "%.120s: %.60s", what, why);
+}
+
+void note_cuda_error(const char* what, cudaError_t e) { note_error(what, cudaGetErrorName(e)); }
+
 // --- device and driver entry points ---------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
 std::once_flag g_encode_once;
+
+void* driver_entry(const char* name, int version) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return fn;
+  cudaGetLastError();
+  return nullptr;
+}
 
 struct DevInfo {
   bool known;
@@ -154,16 +177,27 @@ flce_status current_device(int* sms) {
   if (!g_dev[dev].ok) return FLCE_ERR_UNSUPPORTED_DEVICE;
   *sms = g_dev[dev].sms;
   std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    else
-      cudaGetLastError();
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(driver_entry("cuTensorMapEncodeTiled", 12000));
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_entry("cuCtxGetCurrent", 4000));
   });
-  return g_encode ? FLCE_OK : FLCE_ERR_CUDA;
+  if (!g_encode || !g_ctx_current) {
+    note_error("cudaGetDriverEntryPointByVersion", "cuTensorMapEncodeTiled or cuCtxGetCurrent not found");
+    return FLCE_ERR_CUDA;
+  }
+  // A thread that has made no CUDA call yet (a framework's worker thread, say) has no
+  // current context, and the tensor-map encoder, a driver call, needs one: bind the
+  // device's primary context, as the runtime's own calls would. A context the caller
+  // made current is left alone.
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    const cudaError_t e = cudaSetDevice(dev);
+    if (e != cudaSuccess) {
+      note_cuda_error("cudaSetDevice", e);
+      cudaGetLastError();
+      return FLCE_ERR_CUDA;
+    }
+  }
+  return FLCE_OK;
 }
 
 // 2-D row-major tensor [outer][inner] with row pitch `pitch_elems`, 128-byte swizzled boxes.
@@ -175,7 +209,8 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const voi
   const cuuint32_t es[2] = {1, 1};
   return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS ||
+         (note_error("cuTensorMapEncodeTiled", "the tensor map was refused"), false);
 }
 
 flce_status check_common(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
@@ -211,12 +246,14 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
   *S_out = int(S);
 }
 
-#define FLCE_CUDA_CHECK(expr)                 \
-  do {                                        \
-    if ((expr) != cudaSuccess) {              \
-      cudaGetLastError();                     \
-      return FLCE_ERR_CUDA;                   \
-    }                                         \
+#define FLCE_CUDA_CHECK(expr)                    \
+  do {                                           \
+    const cudaError_t flce_e_ = (expr);          \
+    if (flce_e_ != cudaSuccess) {                \
+      note_cuda_error(#expr, flce_e_);           \
+      cudaGetLastError();                        \
+      return FLCE_ERR_CUDA;                      \
+    }                                            \
   } while (0)
 
 }  // namespace
@@ -224,6 +261,8 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
 extern "C" {
 
 int flce_version(void) { return 100; }
+
+const char* flce_last_error_detail(void) { return g_detail; }
 
 const char* flce_status_string(flce_status st) {
   switch (st) {
@@ -261,7 +300,10 @@ struct Problem {
   int32_t ignore_index;
   float eps, zscale;
   flce_reduction red;
+  bool w_vd;  // W (and dW) stored [V, D] (nn.Linear's weight layout); else [D, V]
 };
+
+bool opt_w_vd(const flce_options* o) { return o && o->weight_layout == FLCE_WEIGHT_VD; }
 
 bool opt_ext_forward(const flce_options* o) {
   return o && (o->softcap > 0.f || o->bias || o->class_weight || o->predicted || o->accuracy);
@@ -278,6 +320,7 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
     return FLCE_ERR_ALIGNMENT;
   if (o->dbias && !o->bias) return FLCE_ERR_INVALID_ARG;
   if (o->row_band < 0) return FLCE_ERR_INVALID_ARG;
+  if (o->weight_layout != FLCE_WEIGHT_DV && o->weight_layout != FLCE_WEIGHT_VD) return FLCE_ERR_INVALID_ARG;
   const bool shard = o->v_total != 0 && o->v_total != pb.V;
   if (shard) {
     if (!backward) return FLCE_ERR_INVALID_ARG;  // forward shards go through flce_shard_stats
@@ -300,11 +343,15 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   int gN = 1, S = 1;
   pick_forward_grid(units, n_tiles, v_tiles, L.S_alloc, &gN, &S);
 
+  // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;
+  const bool enc_w = pb.w_vd ? encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.D),
+                                         uint64_t(pb.V), uint64_t(pb.D), 64, uint32_t(gemm_b_rows_per_cta()))
+                             : encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V),
+                                         uint64_t(pb.D), uint64_t(pb.V), 64, 64);
   if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
                  64, kBM) ||
-      !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
-                 64, 64))
+      !enc_w)
     return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
@@ -336,7 +383,7 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
     p.softcap = opt->softcap;
     p.part_idx = want_idx ? reinterpret_cast<int*>(ws + L.part_idx) : nullptr;
   }
-  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, ext, stream));
+  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, ext, pb.w_vd, stream));
 
   FinalizeParams f{};
   f.mode = mode;
@@ -397,14 +444,18 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const float* cw = opt ? opt->class_weight : nullptr;
   const bool ext = opt_ext_grad(opt);
 
-  // maps that do not depend on the row band
-  CUtensorMap tmWmn, tmWk, tmDW;
-  if (!encode_2d(&tmWmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
-                 64, 64) ||
-      !encode_2d(&tmWk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V),
-                 64, uint32_t(gemm_b_rows_per_cta())) ||
-      !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 32,
-                 kBM))
+  // Maps that do not depend on the row band. tmWg: B of the gradient GEMM (N = vocabulary,
+  // K = D); tmWx: B of the dX GEMM (N = D, K = vocabulary). Each is MN-major in one W layout
+  // and K-major in the other; K-major boxes are 64 x (rows per CTA), MN-major ones 64 x 64.
+  const uint64_t w_inner = pb.w_vd ? uint64_t(pb.D) : uint64_t(pb.V);
+  const uint64_t w_outer = pb.w_vd ? uint64_t(pb.V) : uint64_t(pb.D);
+  const uint32_t kmaj_rows = uint32_t(gemm_b_rows_per_cta());
+  CUtensorMap tmWg, tmWx, tmDW;
+  if (!encode_2d(&tmWg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, w_inner, w_outer, w_inner, 64,
+                 pb.w_vd ? kmaj_rows : 64) ||
+      !encode_2d(&tmWx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, w_inner, w_outer, w_inner, 64,
+                 pb.w_vd ? 64 : kmaj_rows) ||
+      !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, w_inner, w_outer, w_inner, 32, kBM))
     return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
@@ -429,7 +480,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   FLCE_CUDA_CHECK(launch_denominator(pp, stream));  // g over every row of the batch
 
   const int64_t mc = gemm_pairs_per_cluster();
-  const int64_t d_tiles_m = cdiv(cdiv(pb.D, gemm_tile_rows()), mc);  // dW row-tile groups
+  const int64_t d_tiles_m = cdiv(cdiv(pb.D, gemm_tile_rows()), mc);  // dW [D, V]: row-tile groups
   const int64_t d_tiles_n = cdiv(pb.D, kBN);                         // dX columns
   for (int64_t n0 = 0; n0 < pb.N; n0 += Nb) {
     const int64_t nb = (pb.N - n0 < Nb) ? pb.N - n0 : Nb;
@@ -475,7 +526,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         ge.cw = cw;
         ge.softcap = opt->softcap;
       }
-      FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWmn, tmG, wg, ge, ext, stream));
+      FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWg, tmG, wg, ge, ext, pb.w_vd, stream));
 
       if (opt && opt->dbias) {
         ColsumParams cp{};
@@ -490,20 +541,33 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         FLCE_CUDA_CHECK(launch_colsum(cp, stream));
       }
 
+      // dW = X^T G (K = rows of the band); later row bands add into dW. For a [V, D] dW the
+      // GEMM computes G^T X instead: the operands swap, rows are vocabulary tiles.
       WalkParams ww{};
-      ww.total_tiles = int(vt * d_tiles_m);
-      ww.tiles_minor = int(d_tiles_m);
       ww.num_kb = int(cdiv(nb, kBK));
-      StoreEpiParams sw{n0 > 0 ? 1 : 0, int(v0), err};  // later row bands add into dW
-      FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
+      StoreEpiParams sw{n0 > 0 ? 1 : 0, 0, err, 0};
+      if (!pb.w_vd) {
+        ww.total_tiles = int(vt * d_tiles_m);
+        ww.tiles_minor = int(d_tiles_m);
+        ww.col_major = 1;
+        sw.x_off = int(v0);
+        FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
+      } else {
+        const int64_t v_groups = cdiv(cdiv(vc, gemm_tile_rows()), mc);
+        ww.total_tiles = int(v_groups * d_tiles_n);
+        ww.tiles_minor = int(d_tiles_n);
+        ww.col_major = 0;
+        sw.y_off = int(v0);
+        FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDW, ww, sw, stream));
+      }
 
       WalkParams wx{};
       wx.total_tiles = int(n_tiles * d_tiles_n);
       wx.tiles_minor = int(d_tiles_n);
       wx.num_kb = int(cdiv(vc, kBK));
       wx.b_k0 = int(v0);
-      StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err};
-      FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWk, tmDX, wx, sx, stream));
+      StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err, 0};
+      FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, stream));
     }
     if (!f32_out) {
       void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;
@@ -539,14 +603,17 @@ flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets
                             struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
   if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   int sms = 0;
   if ((st = current_device(&sms)) != FLCE_OK) return st;
   const int units = forward_max_units();
-  if (units <= 0) return FLCE_ERR_CUDA;
+  if (units <= 0) {
+    note_error("forward_max_units", "no resident cluster");
+    return FLCE_ERR_CUDA;
+  }
   return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), true, units,
                      reinterpret_cast<cudaStream_t>(stream));
 }
@@ -564,7 +631,7 @@ flce_status flce_backward_ex(const void* X, const void* W, const int32_t* target
                              void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, true)) != FLCE_OK) return st;
   if (ws_bytes < bwd_layout(backward_rows(opt, N), D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
@@ -589,7 +656,7 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
                                   struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red};
+  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
@@ -600,7 +667,10 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
   int sms = 0;
   if ((st = current_device(&sms)) != FLCE_OK) return st;
   const int units = forward_max_units();
-  if (units <= 0) return FLCE_ERR_CUDA;
+  if (units <= 0) {
+    note_error("forward_max_units", "no resident cluster");
+    return FLCE_ERR_CUDA;
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, true, units, s)) != FLCE_OK) return st;
@@ -620,8 +690,11 @@ flce_status flce_shard_stats(const void* X, const void* W, const int32_t* target
   int sms = 0;
   if ((st = current_device(&sms)) != FLCE_OK) return st;
   const int units = forward_max_units();
-  if (units <= 0) return FLCE_ERR_CUDA;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM};
+  if (units <= 0) {
+    note_error("forward_max_units", "no resident cluster");
+    return FLCE_ERR_CUDA;
+  }
+  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, false};
   return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
                      static_cast<uint8_t*>(workspace), true, units, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -671,12 +744,9 @@ flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream_
   if (!workspace) return FLCE_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   int word = 0;
-  if (cudaStreamSynchronize(stream) != cudaSuccess ||
-      cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) {
-    cudaGetLastError();
-    return FLCE_ERR_CUDA;
-  }
+  FLCE_CUDA_CHECK(cudaStreamSynchronize(stream));
+  FLCE_CUDA_CHECK(cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost));
+  FLCE_CUDA_CHECK(cudaMemset(workspace, 0, sizeof(int)));
   if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
   if (word & FLCE_DEVERR_BAD_TARGET) return FLCE_ERR_BAD_TARGET;
   return FLCE_OK;

@@ -154,9 +154,11 @@ struct FwdSched {
   }
 };
 
-// Static round-robin walk for the backward GEMMs. Tile index i = major * minor_count + minor.
+// Static round-robin walk for the backward GEMMs. Tile index i = major * minor_count + minor;
+// the host picks the order (col_major):
 //   WALK_GRAD: major = row tile of X, minor = 256-column vocabulary tile of the band.
-//   WALK_DW  : major = 256-column vocabulary tile, minor = row tile of D.
+//   WALK_DW  : W [D, V]: major = 256-column vocabulary tile, minor = row tile of D;
+//              W [V, D]: major = 256-row vocabulary tile, minor = 256-column tile of D.
 //   WALK_DX  : major = row tile of the band, minor = 256-column tile of D.
 // Row tiles are kBM * CG rows (this CTA takes rows rank*128 .. rank*128+127 of each).
 // With MC pairs per cluster the row-tile index counts groups of MC row tiles (one per
@@ -176,8 +178,8 @@ struct WalkSched {
     if (i >= w.total_tiles) return false;
     const int major = i / w.tiles_minor;
     const int minor = i - major * w.tiles_minor;
-    const int rows = ((KIND == WALK_DW) ? minor : major) * MC + pair;
-    const int cols = (KIND == WALK_DW) ? major : minor;
+    const int rows = (w.col_major ? minor : major) * MC + pair;
+    const int cols = w.col_major ? major : minor;
     t.a_row = rows * Geo<CG>::kTileRows + rank * kBM;
     t.b_row = w.b_row_off + cols * kBN;
     t.a_k0 = w.a_k0;
@@ -638,7 +640,7 @@ __device__ __forceinline__ void online_update_ext(RowStatsExt& st, const uint32_
   }
 }
 
-template <int CG, int MC, int STAGES, bool EXT>
+template <int CG, int MC, int STAGES, bool B_MN, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_forward_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const FwdParams p) {
@@ -659,10 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx w{s.abort_flag, p.err};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG, MC, STAGES, false, true, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, p, w, pr);
+    if (lane == 0) producer_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, p, w, pr);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role<CG, MC, STAGES, false, true, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
+      mma_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
@@ -899,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
           epi_store_box(
               s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
-              sp.x_off + t.b_row + c, t.a_row, sp.reduce_add != 0, store_hint, pol_store);
+              sp.x_off + t.b_row + c, sp.y_off + t.a_row, sp.reduce_add != 0, store_hint, pol_store);
         }
       }
       acc ^= 1;
@@ -961,12 +963,15 @@ int max_clusters(Kern kernel, size_t smem, int slot) {
   return n;
 }
 
-template <bool EXT>
-auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, EXT>; }
-template <bool EXT>
-auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, true, WALK_GRAD, 0, EXT>; }
+// B_MN: W [D, V] is the MN-major B operand of the forward and gradient GEMMs and the
+// K-major B of the dX GEMM; W [V, D] is the other way round.
+template <bool B_MN, bool EXT>
+auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, B_MN, EXT>; }
+template <bool B_MN, bool EXT>
+auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, WALK_GRAD, 0, EXT>; }
 auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, WALK_DW, 1, false>; }
-auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, false, WALK_DX, 1, false>; }
+template <bool B_MN>
+auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, WALK_DX, 1, false>; }
 
 constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
 constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
@@ -994,12 +999,13 @@ int gemm_pairs_per_cluster() { return kMC; }
 
 int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
 
-// Both forward instantiations share the launch shape (same shared memory and threads).
-int forward_max_units() { return max_clusters(fwd_kernel<false>(), kFwdSmem, 0); }
+// Every forward instantiation has the same launch shape (shared memory and threads).
+int forward_max_units() { return max_clusters(fwd_kernel<true, false>(), kFwdSmem, 0); }
 
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
-                                cudaStream_t stream) {
-  auto kern = ext ? fwd_kernel<true>() : fwd_kernel<false>();
+                                bool w_vd, cudaStream_t stream) {
+  auto kern = w_vd ? (ext ? fwd_kernel<false, true>() : fwd_kernel<false, false>())
+                   : (ext ? fwd_kernel<true, true>() : fwd_kernel<true, false>());
   cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -1008,10 +1014,14 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 }
 
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, bool ext, cudaStream_t stream) {
-  StoreEpiParams unused{0, 0, e.err};
-  if (ext) return launch_walk(grad_kernel<true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
-  return launch_walk(grad_kernel<false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, cudaStream_t stream) {
+  StoreEpiParams unused{0, 0, e.err, 0};
+  if (w_vd) {
+    if (ext) return launch_walk(grad_kernel<false, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+    return launch_walk(grad_kernel<false, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  }
+  if (ext) return launch_walk(grad_kernel<true, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  return launch_walk(grad_kernel<true, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
@@ -1022,10 +1032,11 @@ cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 }
 
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, cudaStream_t stream) {
   GradEpiParams unused{};
   unused.err = e.err;
-  return launch_walk(dx_kernel(), tmA, tmB, tmC, w, unused, e, 3, stream);
+  if (w_vd) return launch_walk(dx_kernel<true>(), tmA, tmB, tmC, w, unused, e, 3, stream);
+  return launch_walk(dx_kernel<false>(), tmA, tmB, tmC, w, unused, e, 3, stream);
 }
 
 }  // namespace flce

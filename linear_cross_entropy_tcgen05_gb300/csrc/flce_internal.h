@@ -61,6 +61,8 @@ struct WalkParams {
   int num_kb;        // 64-wide K blocks per tile
   int a_k0, b_k0;    // K coordinate of the first block (A, B)
   int b_row_off;     // added to the B operand's row/column coordinate
+  int col_major;     // 1: the slow index runs over output columns (all row tiles of a
+                     // column in flight), 0: over row-tile groups
 };
 
 // Sentinel target of an ignored row in the per-row gradient coefficients.
@@ -103,6 +105,7 @@ struct StoreEpiParams {
   int reduce_add;  // 0: store, 1: element-wise add into the destination
   int x_off;       // added to the B-row coordinate to form the destination column
   int* err;
+  int y_off;       // added to the A-row coordinate to form the destination row
 };
 
 enum FinalizeMode : int { FIN_LOSS = 0, FIN_SHARD_STATS = 1, FIN_COMBINE = 2 };
@@ -173,8 +176,9 @@ int gemm_b_rows_per_cta();
 int forward_max_units();
 
 // ext: the extended epilogue (bias, softcap, class weights, argmax); else the plain one.
+// w_vd: W is stored [V, D] (B is K-major); else [D, V] (B is MN-major).
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
-                                cudaStream_t stream);
+                                bool w_vd, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream);
 // g and B from the mean denominator over all rows (one block).
 cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream);
@@ -185,12 +189,15 @@ cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream);
 // Column sums of a bf16 band, fixed order (two kernels).
 cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream);
 // The walk GEMMs size their own grids: min(tiles, resident CTA pairs) clusters of 2.
+// w_vd as in launch_forward_gemm: it sets the major-ness of W, the B operand of the
+// gradient and dX GEMMs. The dW GEMM takes both operands MN-major in either layout (the
+// caller swaps them for a [V, D] dW).
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, bool ext, cudaStream_t stream);
+                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, cudaStream_t stream);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, cudaStream_t stream);
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, int num_sms, cudaStream_t stream);
 
 constexpr int kFinalizeThreads = 256;

@@ -137,6 +137,26 @@ def test_refuses_without_a_supported_device(lib):
     assert _bwd(lib) == 3
 
 
+def test_options_struct_matches_the_header():
+    """Field order and offsets of flce_options as declared in flce.h (the ctypes mirror)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct flce_options \{(.*?)\} flce_options;", text, flags=re.S).group(1)
+    names = re.findall(r"(\w+);", body)
+    assert names == [f[0] for f in flce.FlceOptions._fields_]
+    assert flce.make_options(weight_layout="vd").weight_layout == 1
+    assert flce.make_options().weight_layout == 0
+
+
+def test_python_wrapper_checks_the_weight_layout_shape():
+    X = torch.zeros(4, 8, dtype=torch.bfloat16)
+    Wvd = torch.zeros(16, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match=r"W \[D,V\]"):
+        flce.linear_cross_entropy(X, Wvd, y)                       # [V, D] passed as [D, V]
+    with pytest.raises(ValueError, match="CUDA"):
+        flce.linear_cross_entropy(X, Wvd, y, weight_layout="vd")  # shapes fine, CPU tensors refused
+
+
 def test_python_wrapper_validates_dtypes():
     X = torch.zeros(4, 8, dtype=torch.float32)
     W = torch.zeros(8, 16, dtype=torch.bfloat16)
@@ -172,6 +192,8 @@ def test_option_checks(lib):
     assert _bwd_ex(lib, _opts(v_offset=1000, v_total=1500)) == 1  # shard beyond the vocabulary
     assert _bwd_ex(lib, _opts(bias=0xA0000, v_offset=0, v_total=4096)) == 1  # shards take no bias
     assert _bwd_ex(lib, _opts(dX_f32=0xA0008)) == 2         # fp32 dX needs 16-byte alignment
+    assert _fwd_ex(lib, _opts(weight_layout=2)) == 1        # not a flce_weight_layout
+    assert _bwd_ex(lib, _opts(weight_layout=-1)) == 1
     assert lib.flce_combine_shards(0x10000, 0, 0x30000, 256, 1024, -100, 0.0, 0.0, 0, 0x40000, 0x50000,
                                    0x60000, 1 << 20, None) == 1   # K >= 1
     assert lib.flce_shard_stats(0x10000, 0x20000, 0x30000, 256, 128, 1024, -8, -100, 0x40000, 0x60000,

@@ -284,9 +284,14 @@ __device__ __forceinline__ void tmem_teardown(uint32_t tmem_base, int warp) {
 // re-reads (W in the backward GEMMs) stays, the streamed one goes first.
 template <int KIND>
 struct OperandPolicy {
-  static constexpr int A = FLCE_L2_HINTS && KIND == WALK_DX ? POL_EVICT_FIRST : POL_NORMAL;
-  static constexpr int B = FLCE_L2_HINTS && (KIND == WALK_GRAD || KIND == WALK_DX) ? POL_EVICT_LAST : POL_NORMAL;
-  static constexpr int STORE = FLCE_L2_HINTS && KIND == WALK_GRAD ? POL_EVICT_FIRST : POL_NORMAL;
+  static constexpr int A = !FLCE_L2_HINTS ? POL_NORMAL
+                           : KIND == WALK_DX ? FLCE_DX_A_POL
+                           : KIND == WALK_DW ? FLCE_DW_A_POL
+                                             : POL_NORMAL;
+  static constexpr int B = !FLCE_L2_HINTS ? POL_NORMAL
+                           : (KIND == WALK_GRAD || KIND == WALK_DX) ? POL_EVICT_LAST
+                                                                    : FLCE_DW_B_POL;
+  static constexpr int STORE = FLCE_L2_HINTS && KIND == WALK_GRAD ? FLCE_GRAD_STORE_POL : POL_NORMAL;
 };
 constexpr int KIND_FWD = -1;
 template <>

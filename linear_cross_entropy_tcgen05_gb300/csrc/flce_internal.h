@@ -46,6 +46,20 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_PAIRS_PER_CLUSTER
 #define FLCE_PAIRS_PER_CLUSTER 2
 #endif
+// L2 policies (0 normal, 1 evict-first, 2 evict-last) of the dX GEMM's A operand (the
+// gradient band), the dW GEMM's operands, and the gradient GEMM's band store.
+#ifndef FLCE_DX_A_POL
+#define FLCE_DX_A_POL 0
+#endif
+#ifndef FLCE_DW_A_POL
+#define FLCE_DW_A_POL 0
+#endif
+#ifndef FLCE_DW_B_POL
+#define FLCE_DW_B_POL 0
+#endif
+#ifndef FLCE_GRAD_STORE_POL
+#define FLCE_GRAD_STORE_POL 1
+#endif
 // L2 cache-policy hints on the GEMMs' TMA traffic (1: on).
 #ifndef FLCE_L2_HINTS
 #define FLCE_L2_HINTS 1

@@ -161,6 +161,19 @@ def oracle_sample_rate(wl, X, W, y, rows: int):
     return rows / dt, dt
 
 
+def oracle_sample_for(wl, X, W, y, seconds: float, chunk: int = 256):
+    """fp64 oracle fwd+bwd over successive chunks of rows (full vocabulary) until `seconds`
+    of CPU time have passed or every row is done; returns (tokens/s, rows, seconds)."""
+    rows, dt = 0, 0.0
+    while rows < X.shape[0] and (rows == 0 or dt < seconds):
+        n = min(chunk, X.shape[0] - rows)
+        sl = slice(rows, rows + n)
+        r, t = oracle_sample_rate(wl, X[sl], W, y[sl], n)
+        rows += n
+        dt += t
+    return rows / dt, rows, dt
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -374,9 +387,10 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
         return
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        rate, dt = oracle_sample_rate(wl, X, W, y, args.oracle_rows)
+        rate, rows, dt = oracle_sample_for(wl, X, W, y, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"fp64 oracle fwd+bwd of {args.oracle_rows} rows x full V ({dt:.1f} s); tokens/s = rows/time"}
+               "sample": f"fp64 oracle fwd+bwd of the first {rows} rows x full V in chunks of 256 "
+                         f"({dt:.1f} s); tokens/s = rows/time"}
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "forward_gemm_traffic.json")
     if os.path.exists(tr_path):
@@ -432,7 +446,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline", choices=sorted(WORKLOADS))
-    ap.add_argument("--oracle-rows", type=int, default=512)
+    ap.add_argument("--oracle-rows", type=int, default=512, help="rows per step of the reference arm")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU time of the cpu_baseline sample")
     ap.add_argument("--shape", default=None, help="N,D,V override of the workload's shape (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")

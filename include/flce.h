@@ -147,6 +147,14 @@ flce_status flce_backward(const void* X, const void* W, const int32_t* targets, 
  * head, taken as it is stored (no transposed copy). Not a part of the pages' method. */
 typedef enum { FLCE_WEIGHT_DV = 0, FLCE_WEIGHT_VD = 1 } flce_weight_layout;
 
+/* Element type of X and W (and of dX; dW is fp32 either way). The tensor cores multiply
+ * both at the same rate. With f16 the gradient band holds G/g scaled by 2^10 (so that
+ * probabilities near 1/V stay normal f16 numbers) and dX, dW are scaled back in fp32; this
+ * needs (1 - eps) w_y + (eps/V) sum_j w_j + 2 s lse < 64 on every row (class weights below
+ * ~60 in practice), else the band overflows to inf. Not a part of the pages' method, whose
+ * kernels take 16-bit inputs ([P4] "Summary"). */
+typedef enum { FLCE_INPUT_BF16 = 0, FLCE_INPUT_F16 = 1 } flce_input_dtype;
+
 typedef struct flce_options {
   float softcap;             /* > 0: cap the logits with softcap*tanh(z/softcap); 0: off */
   const float* bias;         /* device fp32 [V] added to every row's logits, or NULL */
@@ -162,6 +170,7 @@ typedef struct flce_options {
                                 flce_workspace_size(row_band, D, V, 1) whatever N is; dW then
                                 accumulates across bands (fp32 adds in a fixed order). 0: all rows. */
   int32_t weight_layout;     /* flce_weight_layout of W and dW (FLCE_WEIGHT_DV if 0) */
+  int32_t input_dtype;       /* flce_input_dtype of X, W and dX (FLCE_INPUT_BF16 if 0) */
 } flce_options;
 
 /* flce_forward with options (NULL behaves exactly like flce_forward). Vocabulary

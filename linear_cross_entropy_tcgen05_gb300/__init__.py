@@ -10,6 +10,8 @@ the library is missing, ``load_library`` raises.
 ``linear_cross_entropy`` wraps the two calls in a ``torch.autograd.Function``. W is
 [D, V] by default; ``weight_layout="vd"`` takes the [V, D] weight of an
 ``nn.Linear(D, V, bias=False)`` language-model head as it is (dW then has that layout too).
+X and W are bf16, or both f16 (``input_dtype="f16"`` in the options of the ``_ex`` calls;
+the autograd wrapper picks it from the tensors).
 """
 from __future__ import annotations
 
@@ -23,7 +25,7 @@ __all__ = [
     "flce_check_device_error", "flce_status_string", "flce_version", "linear_cross_entropy",
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
-    "flce_combine_shards", "WEIGHT_LAYOUTS", "flce_last_error_detail",
+    "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,6 +33,7 @@ _LIB = None
 
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 WEIGHT_LAYOUTS = {"dv": 0, "vd": 1}  # flce_weight_layout: W [D, V] or W [V, D]
+INPUT_DTYPES = {"bf16": 0, "f16": 1}  # flce_input_dtype of X, W and dX
 STATUS = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_ALIGNMENT", 3: "FLCE_ERR_UNSUPPORTED_DEVICE",
     4: "FLCE_ERR_WORKSPACE_TOO_SMALL", 5: "FLCE_ERR_REDUCTION_NONE_GRAD", 6: "FLCE_ERR_CUDA",
@@ -48,19 +51,37 @@ class FlceOptions(ctypes.Structure):
     _fields_ = [("softcap", ctypes.c_float), ("bias", ctypes.c_void_p), ("class_weight", ctypes.c_void_p),
                 ("predicted", ctypes.c_void_p), ("accuracy", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
                 ("dX_f32", ctypes.c_void_p), ("v_offset", ctypes.c_int64), ("v_total", ctypes.c_int64),
-                ("row_band", ctypes.c_int64), ("weight_layout", ctypes.c_int32)]
+                ("row_band", ctypes.c_int64), ("weight_layout", ctypes.c_int32), ("input_dtype", ctypes.c_int32)]
 
 
 def _layout(weight_layout) -> int:
     return WEIGHT_LAYOUTS[weight_layout] if isinstance(weight_layout, str) else int(weight_layout)
 
 
+def _dtype_code(input_dtype) -> int:
+    if isinstance(input_dtype, torch.dtype):
+        return {torch.bfloat16: 0, torch.float16: 1}[input_dtype]
+    return INPUT_DTYPES[input_dtype] if isinstance(input_dtype, str) else int(input_dtype)
+
+
 def make_options(softcap: float = 0.0, bias=None, class_weight=None, predicted=None, accuracy=None, dbias=None,
-                 dX_f32=None, v_offset: int = 0, v_total: int = 0, row_band: int = 0, weight_layout="dv"):
+                 dX_f32=None, v_offset: int = 0, v_total: int = 0, row_band: int = 0, weight_layout="dv",
+                 input_dtype="bf16"):
     """An ``flce_options`` value (device tensors become pointers)."""
     return FlceOptions(float(softcap), _ptr(bias), _ptr(class_weight), _ptr(predicted), _ptr(accuracy),
                        _ptr(dbias), _ptr(dX_f32), int(v_offset), int(v_total), int(row_band),
-                       _layout(weight_layout))
+                       _layout(weight_layout), _dtype_code(input_dtype))
+
+
+def _check_dtype(X, options) -> None:
+    """The options must name X's element type (the library cannot see it)."""
+    if not isinstance(X, torch.Tensor):
+        return
+    want = 1 if X.dtype == torch.float16 else 0
+    have = options.input_dtype if options is not None else 0
+    if want != have:
+        raise TypeError(f"X is {X.dtype} but the options say input_dtype={have}: "
+                        "pass make_options(input_dtype=X.dtype)")
 
 
 def _vocab(W, options) -> int:
@@ -172,6 +193,7 @@ def flce_forward(X, W, targets, loss, lse, workspace, ignore_index: int = -100, 
                  zloss_scale: float = 0.0, reduction: str = "mean", stream=None, N=None, D=None, V=None,
                  ws_bytes=None, raise_on_error: bool = True) -> int:
     """Call flce_forward. Tensors are device tensors laid out as in flce.h; returns the status."""
+    _check_dtype(X, None)
     N = X.shape[0] if N is None else N
     D = X.shape[1] if D is None else D
     V = W.shape[1] if V is None else V
@@ -188,6 +210,7 @@ def flce_backward(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_index:
                   label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean", stream=None,
                   N=None, D=None, V=None, ws_bytes=None, raise_on_error: bool = True) -> int:
     """Call flce_backward (grad_out is a device fp32 scalar tensor); returns the status."""
+    _check_dtype(X, None)
     N = X.shape[0] if N is None else N
     D = X.shape[1] if D is None else D
     V = W.shape[1] if V is None else V
@@ -213,6 +236,7 @@ def flce_forward_ex(X, W, targets, loss, lse, workspace, ignore_index: int = -10
                     zloss_scale: float = 0.0, reduction: str = "mean", options: FlceOptions | None = None,
                     stream=None, raise_on_error: bool = True) -> int:
     """Call flce_forward_ex (``options`` from ``make_options``)."""
+    _check_dtype(X, options)
     st = load_library().flce_forward_ex(
         _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(loss), _ptr(lse),
@@ -226,6 +250,7 @@ def flce_backward_ex(X, W, targets, lse, grad_out, dX, dW, workspace, ignore_ind
                      label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean",
                      options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
     """Call flce_backward_ex (dX may be None when options.dX_f32 is set)."""
+    _check_dtype(X, options)
     st = load_library().flce_backward_ex(
         _ptr(X), _ptr(W), _ptr(targets), _ptr(lse), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(dX),
@@ -239,6 +264,7 @@ def flce_forward_backward(X, W, targets, grad_out, loss, lse, dX, dW, workspace,
                           label_smoothing: float = 0.0, zloss_scale: float = 0.0, reduction: str = "mean",
                           options: FlceOptions | None = None, stream=None, raise_on_error: bool = True) -> int:
     """Call flce_forward_backward (workspace: flce_workspace_size(N, D, V, 2) bytes)."""
+    _check_dtype(X, options)
     st = load_library().flce_forward_backward(
         _ptr(X), _ptr(W), _ptr(targets), X.shape[0], X.shape[1], _vocab(W, options), int(ignore_index),
         float(label_smoothing), float(zloss_scale), _red(reduction), _opt_ref(options), _ptr(grad_out), _ptr(loss),
@@ -285,8 +311,8 @@ def _workspace(N, D, V, device, for_backward, cache=None):
 
 
 def _validate(X, W, targets, layout=0):
-    if X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
-        raise TypeError("X and W must be bfloat16")
+    if X.dtype not in (torch.bfloat16, torch.float16) or W.dtype != X.dtype:
+        raise TypeError("X and W must both be bfloat16 or both float16")
     if targets.dtype != torch.int32:
         raise TypeError("targets must be int32")
     wd = W.shape[1] if layout == 1 else W.shape[0]
@@ -314,7 +340,7 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         lse = torch.empty(N, dtype=torch.float32, device=X.device)
         b32 = bias.detach().float().contiguous() if bias is not None else None
         w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout)
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout, input_dtype=X.dtype)
         flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction, opts)
         ctx.save_for_backward(X, W, targets, lse)
         ctx.extra = (b32, w32, bias is not None and bias.requires_grad, bias.dtype if bias is not None else None)
@@ -335,7 +361,8 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         dX = torch.empty_like(X)
         dW = torch.empty(W.shape, dtype=torch.float32, device=X.device)
         db = torch.empty(V, dtype=torch.float32, device=X.device) if want_db else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db, weight_layout=layout)
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db, weight_layout=layout,
+                            input_dtype=X.dtype)
         flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction,
                          opts)
         return (dX, dW.to(W.dtype), None, None, None, None, None, None,
@@ -345,7 +372,7 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
 def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,
                          zloss_scale: float = 0.0, reduction: str = "mean", softcap: float = 0.0, bias=None,
                          class_weight=None, weight_layout: str = "dv"):
-    """Fused linear cross-entropy of X [N,D] (bf16), W [D,V] (bf16), int32 targets [N].
+    """Fused linear cross-entropy of X [N,D], W [D,V] (both bf16 or both f16), int32 targets [N].
 
     ``weight_layout="vd"`` takes W as [V,D] (an ``nn.Linear(D, V)`` weight) instead.
 

@@ -301,9 +301,15 @@ struct Problem {
   float eps, zscale;
   flce_reduction red;
   bool w_vd;  // W (and dW) stored [V, D] (nn.Linear's weight layout); else [D, V]
+  bool f16;   // X and W (and dX) are f16; else bf16
+  // tensor-map element type of X, W and the gradient band
+  CUtensorMapDataType dt16() const {
+    return f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  }
 };
 
 bool opt_w_vd(const flce_options* o) { return o && o->weight_layout == FLCE_WEIGHT_VD; }
+bool opt_f16(const flce_options* o) { return o && o->input_dtype == FLCE_INPUT_F16; }
 
 bool opt_ext_forward(const flce_options* o) {
   return o && (o->softcap > 0.f || o->bias || o->class_weight || o->predicted || o->accuracy);
@@ -321,6 +327,7 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
   if (o->dbias && !o->bias) return FLCE_ERR_INVALID_ARG;
   if (o->row_band < 0) return FLCE_ERR_INVALID_ARG;
   if (o->weight_layout != FLCE_WEIGHT_DV && o->weight_layout != FLCE_WEIGHT_VD) return FLCE_ERR_INVALID_ARG;
+  if (o->input_dtype != FLCE_INPUT_BF16 && o->input_dtype != FLCE_INPUT_F16) return FLCE_ERR_INVALID_ARG;
   const bool shard = o->v_total != 0 && o->v_total != pb.V;
   if (shard) {
     if (!backward) return FLCE_ERR_INVALID_ARG;  // forward shards go through flce_shard_stats
@@ -345,11 +352,11 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
 
   // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;
-  const bool enc_w = pb.w_vd ? encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.D),
+  const bool enc_w = pb.w_vd ? encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.D),
                                          uint64_t(pb.V), uint64_t(pb.D), 64, uint32_t(gemm_b_rows_per_cta()))
-                             : encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, uint64_t(pb.V),
+                             : encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.V),
                                          uint64_t(pb.D), uint64_t(pb.V), 64, 64);
-  if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
+  if (!encode_2d(&tmX, pb.dt16(), 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
                  64, kBM) ||
       !enc_w)
     return FLCE_ERR_CUDA;
@@ -383,7 +390,7 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
     p.softcap = opt->softcap;
     p.part_idx = want_idx ? reinterpret_cast<int*>(ws + L.part_idx) : nullptr;
   }
-  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, ext, pb.w_vd, stream));
+  FLCE_CUDA_CHECK(launch_forward_gemm(tmX, tmW, p, ext, pb.w_vd, pb.f16, stream));
 
   FinalizeParams f{};
   f.mode = mode;
@@ -443,6 +450,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const int64_t v_offset = shard ? opt->v_offset : 0;
   const float* cw = opt ? opt->class_weight : nullptr;
   const bool ext = opt_ext_grad(opt);
+  const float* out_scale = pb.f16 ? gval : nullptr;  // dW, dX = g / kF16GradScale * (f16 band GEMM)
 
   // Maps that do not depend on the row band. tmWg: B of the gradient GEMM (N = vocabulary,
   // K = D); tmWx: B of the dX GEMM (N = D, K = vocabulary). Each is MN-major in one W layout
@@ -451,9 +459,9 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const uint64_t w_outer = pb.w_vd ? uint64_t(pb.V) : uint64_t(pb.D);
   const uint32_t kmaj_rows = uint32_t(gemm_b_rows_per_cta());
   CUtensorMap tmWg, tmWx, tmDW;
-  if (!encode_2d(&tmWg, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, w_inner, w_outer, w_inner, 64,
+  if (!encode_2d(&tmWg, pb.dt16(), 2, pb.W, w_inner, w_outer, w_inner, 64,
                  pb.w_vd ? kmaj_rows : 64) ||
-      !encode_2d(&tmWx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W, w_inner, w_outer, w_inner, 64,
+      !encode_2d(&tmWx, pb.dt16(), 2, pb.W, w_inner, w_outer, w_inner, 64,
                  pb.w_vd ? 64 : kmaj_rows) ||
       !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, w_inner, w_outer, w_inner, 32, kBM))
     return FLCE_ERR_CUDA;
@@ -476,6 +484,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   pp.coef = coef;
   pp.gval = gval;
   pp.bval = bval;
+  pp.gscale = pb.f16 ? kF16GradScale : 0.f;  // the f16 band holds G / g, scaled
   pp.err = err;
   FLCE_CUDA_CHECK(launch_denominator(pp, stream));  // g over every row of the batch
 
@@ -488,13 +497,13 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
     float* dx_dst = f32_out ? opt->dX_f32 + size_t(n0) * size_t(pb.D) : dx_acc;
     CUtensorMap tmXk, tmXmn, tmG, tmGmn, tmDX;
     const bool enc =
-        encode_2d(&tmXk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
+        encode_2d(&tmXk, pb.dt16(), 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
                   kBM) &&
-        encode_2d(&tmXmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
+        encode_2d(&tmXmn, pb.dt16(), 2, Xb, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D), 64,
                   64) &&
-        encode_2d(&tmG, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
+        encode_2d(&tmG, pb.dt16(), 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
                   kBM) &&
-        encode_2d(&tmGmn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
+        encode_2d(&tmGmn, pb.dt16(), 2, band, uint64_t(Vc), uint64_t(nb), uint64_t(Vc), 64,
                   64) &&
         encode_2d(&tmDX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dx_dst, uint64_t(pb.D), uint64_t(nb), uint64_t(pb.D),
                   32, kBM);
@@ -526,7 +535,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         ge.cw = cw;
         ge.softcap = opt->softcap;
       }
-      FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWg, tmG, wg, ge, ext, pb.w_vd, stream));
+      FLCE_CUDA_CHECK(launch_grad_gemm(tmXk, tmWg, tmG, wg, ge, ext, pb.w_vd, pb.f16, stream));
 
       if (opt && opt->dbias) {
         ColsumParams cp{};
@@ -538,6 +547,9 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         cp.partial = reinterpret_cast<float*>(ws + L.colsum);
         cp.out = opt->dbias + v0;
         cp.accumulate = n0 > 0 ? 1 : 0;
+        cp.f16 = pb.f16 ? 1 : 0;
+        cp.scale = pb.f16 ? gval : nullptr;
+        cp.scale_mul = 1.f / kF16GradScale;
         FLCE_CUDA_CHECK(launch_colsum(cp, stream));
       }
 
@@ -545,20 +557,20 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       // GEMM computes G^T X instead: the operands swap, rows are vocabulary tiles.
       WalkParams ww{};
       ww.num_kb = int(cdiv(nb, kBK));
-      StoreEpiParams sw{n0 > 0 ? 1 : 0, 0, err, 0};
+      StoreEpiParams sw{n0 > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
       if (!pb.w_vd) {
         ww.total_tiles = int(vt * d_tiles_m);
         ww.tiles_minor = int(d_tiles_m);
         ww.col_major = 1;
         sw.x_off = int(v0);
-        FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, stream));
+        FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, pb.f16, stream));
       } else {
         const int64_t v_groups = cdiv(cdiv(vc, gemm_tile_rows()), mc);
         ww.total_tiles = int(v_groups * d_tiles_n);
         ww.tiles_minor = int(d_tiles_n);
         ww.col_major = 0;
         sw.y_off = int(v0);
-        FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDW, ww, sw, stream));
+        FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDW, ww, sw, pb.f16, stream));
       }
 
       WalkParams wx{};
@@ -566,12 +578,12 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       wx.tiles_minor = int(d_tiles_n);
       wx.num_kb = int(cdiv(vc, kBK));
       wx.b_k0 = int(v0);
-      StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err, 0};
-      FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, stream));
+      StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
+      FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, pb.f16, stream));
     }
     if (!f32_out) {
       void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;
-      FLCE_CUDA_CHECK(launch_cast_bf16(dx_acc, dXb, size_t(nb) * size_t(pb.D), sms, stream));
+      FLCE_CUDA_CHECK(launch_cast_16bit(dx_acc, dXb, size_t(nb) * size_t(pb.D), pb.f16, sms, stream));
     }
   }
   return FLCE_OK;
@@ -603,7 +615,8 @@ flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets
                             struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
+  const Problem pb{X,   W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt),
+                   opt_f16(opt)};
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
   if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
@@ -631,7 +644,8 @@ flce_status flce_backward_ex(const void* X, const void* W, const int32_t* target
                              void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
+  const Problem pb{X,   W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt),
+                   opt_f16(opt)};
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, true)) != FLCE_OK) return st;
   if (ws_bytes < bwd_layout(backward_rows(opt, N), D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
@@ -656,7 +670,8 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
                                   struct CUstream_st* stream) {
   flce_status st = check_common(X, W, targets, N, D, V, label_smoothing, zloss_scale, int(red), workspace);
   if (st != FLCE_OK) return st;
-  const Problem pb{X, W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt)};
+  const Problem pb{X,   W, targets, N, D, V, ignore_index, label_smoothing, zloss_scale, red, opt_w_vd(opt),
+                   opt_f16(opt)};
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
@@ -694,7 +709,7 @@ flce_status flce_shard_stats(const void* X, const void* W, const int32_t* target
     note_error("forward_max_units", "no resident cluster");
     return FLCE_ERR_CUDA;
   }
-  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, false};
+  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, false, false};
   return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
                      static_cast<uint8_t*>(workspace), true, units, reinterpret_cast<cudaStream_t>(stream));
 }

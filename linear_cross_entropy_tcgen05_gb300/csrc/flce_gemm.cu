@@ -31,6 +31,7 @@
 //               once) or TMA element-wise add (dX accumulation across vocabulary bands,
 //               each element touched by one tile per launch, so no races).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include <type_traits>
@@ -351,9 +352,9 @@ __device__ __forceinline__ void load_stage(uint8_t* sa, uint8_t* sb, const CUten
   }
 }
 
-template <int CG, bool A_MN, bool B_MN>
+template <int CG, bool A_MN, bool B_MN, bool F16>
 __device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sa, uint32_t sb, bool acc_first) {
-  constexpr uint32_t idesc = make_idesc_bf16(kBM * CG, kBN, A_MN, B_MN);
+  constexpr uint32_t idesc = make_idesc_16bit(kBM * CG, kBN, A_MN, B_MN, F16);
 #pragma unroll
   for (int kk = 0; kk < kBK / 16; ++kk) {
     // K-major: advance 16 elements = 32 bytes inside the swizzled 128-byte row.
@@ -439,7 +440,7 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
   }
 }
 
-template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, int KIND, class Sched, class SP>
+template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, bool F16, int KIND, class Sched, class SP>
 __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, const SP& sp, const WaitCtx& w,
                                          int leader) {
   Sched sched(sp);
@@ -474,7 +475,7 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
 #endif
       tc_fence_after_sync();
       const uint32_t sa = smem_addr(s.stage + stage * Geo<CG>::kStageBytesCta);
-      mma_stage<CG, A_MN, B_MN>(d_tmem, sa, sa + kABytes, kb > 0);
+      mma_stage<CG, A_MN, B_MN, F16>(d_tmem, sa, sa + kABytes, kb > 0);
       issued_any = true;
       commit_stage<CG, MC>(&s.empty[stage]);
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -645,7 +646,7 @@ __device__ __forceinline__ void online_update_ext(RowStatsExt& st, const uint32_
   }
 }
 
-template <int CG, int MC, int STAGES, bool B_MN, bool EXT>
+template <int CG, int MC, int STAGES, bool B_MN, bool F16, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_forward_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const FwdParams p) {
@@ -669,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) producer_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, p, w, pr);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
+      mma_role<CG, MC, STAGES, false, B_MN, F16, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
@@ -797,7 +798,7 @@ __device__ __forceinline__ void epi_store_box(const Smem& s, int epi_tid, uint32
   }
 }
 
-template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, int KIND, int EPI, bool EXT>
+template <int CG, int MC, int STAGES, bool A_MN, bool B_MN, bool F16, int KIND, int EPI, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     flce_walk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                           const __grid_constant__ CUtensorMap tmC, const WalkParams wp, const GradEpiParams gp,
@@ -825,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       producer_role<CG, MC, STAGES, A_MN, B_MN, KIND, WalkSched<CG, MC, KIND>>(s, &tmA, &tmB, wp, w, pr);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0)
-      mma_role<CG, MC, STAGES, A_MN, B_MN, KIND, WalkSched<CG, MC, KIND>>(s, tmem_base, wp, w, pr.leader);
+      mma_role<CG, MC, STAGES, A_MN, B_MN, F16, KIND, WalkSched<CG, MC, KIND>>(s, tmem_base, wp, w, pr.leader);
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);
@@ -886,21 +887,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               gg[h] = (col >= gp.V) ? 0.f : g;
             }
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(gg[0], gg[1]);
-            packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+            if constexpr (F16) {
+              const __half2 hv = __floats2half2_rn(gg[0], gg[1]);
+              packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+            } else {
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(gg[0], gg[1]);
+              packed[j >> 1] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
           }
           epi_store_box(
               s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
               col0 - gp.chunk_v0, t.a_row, false, store_hint, pol_store);
         }
       } else {
-        // fp32 accumulator -> dW (store) or dX accumulator (store / add), 32 columns per box.
+        // fp32 accumulator -> dW (store) or dX accumulator (store / add), 32 columns per box;
+        // with a scaled gradient band (f16 inputs) the accumulator is scaled back first.
+        const float out_scale = sp.scale != nullptr ? __ldg(sp.scale) * sp.scale_mul : 1.f;
 #pragma unroll 1
         for (int c = 0; c < kBN; c += 32) {
           uint32_t r0[32];
           tmem_ld_32cols(taddr + uint32_t(c), r0);
           tc_wait_ld();
           if (c + 32 == kBN) epi_release<CG>(s, acc, pr.leader);
+          if (sp.scale != nullptr) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) r0[q] = __float_as_uint(__uint_as_float(r0[q]) * out_scale);
+          }
           uint4 chunks[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
@@ -970,13 +982,14 @@ int max_clusters(Kern kernel, size_t smem, int slot) {
 
 // B_MN: W [D, V] is the MN-major B operand of the forward and gradient GEMMs and the
 // K-major B of the dX GEMM; W [V, D] is the other way round.
-template <bool B_MN, bool EXT>
-auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, B_MN, EXT>; }
-template <bool B_MN, bool EXT>
-auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, WALK_GRAD, 0, EXT>; }
-auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, WALK_DW, 1, false>; }
-template <bool B_MN>
-auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, WALK_DX, 1, false>; }
+template <bool B_MN, bool F16, bool EXT>
+auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, B_MN, F16, EXT>; }
+template <bool B_MN, bool F16, bool EXT>
+auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, F16, WALK_GRAD, 0, EXT>; }
+template <bool F16>
+auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, F16, WALK_DW, 1, false>; }
+template <bool B_MN, bool F16>
+auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, F16, WALK_DX, 1, false>; }
 
 constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
 constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
@@ -1005,12 +1018,31 @@ int gemm_pairs_per_cluster() { return kMC; }
 int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
 
 // Every forward instantiation has the same launch shape (shared memory and threads).
-int forward_max_units() { return max_clusters(fwd_kernel<true, false>(), kFwdSmem, 0); }
+int forward_max_units() { return max_clusters(fwd_kernel<true, false, false>(), kFwdSmem, 0); }
+
+namespace {
+template <bool F16>
+auto pick_fwd(bool ext, bool w_vd) {
+  return w_vd ? (ext ? fwd_kernel<false, F16, true>() : fwd_kernel<false, F16, false>())
+              : (ext ? fwd_kernel<true, F16, true>() : fwd_kernel<true, F16, false>());
+}
+template <bool F16>
+cudaError_t grad_walk(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const WalkParams& w,
+                      const GradEpiParams& e, bool ext, bool w_vd, cudaStream_t stream) {
+  StoreEpiParams unused{};
+  unused.err = e.err;
+  if (w_vd) {
+    if (ext) return launch_walk(grad_kernel<false, F16, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+    return launch_walk(grad_kernel<false, F16, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  }
+  if (ext) return launch_walk(grad_kernel<true, F16, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+  return launch_walk(grad_kernel<true, F16, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+}
+}  // namespace
 
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
-                                bool w_vd, cudaStream_t stream) {
-  auto kern = w_vd ? (ext ? fwd_kernel<false, true>() : fwd_kernel<false, false>())
-                   : (ext ? fwd_kernel<true, true>() : fwd_kernel<true, false>());
+                                bool w_vd, bool f16, cudaStream_t stream) {
+  auto kern = f16 ? pick_fwd<true>(ext, w_vd) : pick_fwd<false>(ext, w_vd);
   cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -1019,29 +1051,30 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
 }
 
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, cudaStream_t stream) {
-  StoreEpiParams unused{0, 0, e.err, 0};
-  if (w_vd) {
-    if (ext) return launch_walk(grad_kernel<false, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
-    return launch_walk(grad_kernel<false, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
-  }
-  if (ext) return launch_walk(grad_kernel<true, true>(), tmA, tmB, tmC, w, e, unused, 1, stream);
-  return launch_walk(grad_kernel<true, false>(), tmA, tmB, tmC, w, e, unused, 1, stream);
+                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, bool f16,
+                             cudaStream_t stream) {
+  return f16 ? grad_walk<true>(tmA, tmB, tmC, w, e, ext, w_vd, stream)
+             : grad_walk<false>(tmA, tmB, tmC, w, e, ext, w_vd, stream);
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, bool f16, cudaStream_t stream) {
   GradEpiParams unused{};
   unused.err = e.err;
-  return launch_walk(dw_kernel(), tmA, tmB, tmC, w, unused, e, 2, stream);
+  if (f16) return launch_walk(dw_kernel<true>(), tmA, tmB, tmC, w, unused, e, 2, stream);
+  return launch_walk(dw_kernel<false>(), tmA, tmB, tmC, w, unused, e, 2, stream);
 }
 
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, bool f16, cudaStream_t stream) {
   GradEpiParams unused{};
   unused.err = e.err;
-  if (w_vd) return launch_walk(dx_kernel<true>(), tmA, tmB, tmC, w, unused, e, 3, stream);
-  return launch_walk(dx_kernel<false>(), tmA, tmB, tmC, w, unused, e, 3, stream);
+  if (f16) {
+    if (w_vd) return launch_walk(dx_kernel<true, true>(), tmA, tmB, tmC, w, unused, e, 3, stream);
+    return launch_walk(dx_kernel<false, true>(), tmA, tmB, tmC, w, unused, e, 3, stream);
+  }
+  if (w_vd) return launch_walk(dx_kernel<true, false>(), tmA, tmB, tmC, w, unused, e, 3, stream);
+  return launch_walk(dx_kernel<false, false>(), tmA, tmB, tmC, w, unused, e, 3, stream);
 }
 
 }  // namespace flce

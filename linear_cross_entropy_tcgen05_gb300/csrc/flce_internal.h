@@ -116,11 +116,19 @@ struct GradEpiParams {
 };
 
 struct StoreEpiParams {
-  int reduce_add;  // 0: store, 1: element-wise add into the destination
-  int x_off;       // added to the B-row coordinate to form the destination column
+  int reduce_add;      // 0: store, 1: element-wise add into the destination
+  int x_off;           // added to the B-row coordinate to form the destination column
   int* err;
-  int y_off;       // added to the A-row coordinate to form the destination row
+  int y_off;           // added to the A-row coordinate to form the destination row
+  const float* scale;  // null, or the accumulator is multiplied by *scale * scale_mul
+  float scale_mul;
 };
+
+// f16 inputs: the gradient band holds G * kF16GradScale / g (g = the loss scale of the
+// gradient), so that probabilities near 1/V stay normal f16 numbers; the dW and dX
+// epilogues multiply by g / kF16GradScale. |G / g| is at most (1 - eps) w_y +
+// (eps / V) sum_j w_j + 2 s lse, which must stay below 65504 / kF16GradScale = 64.
+constexpr float kF16GradScale = 1024.f;
 
 enum FinalizeMode : int { FIN_LOSS = 0, FIN_SHARD_STATS = 1, FIN_COMBINE = 2 };
 
@@ -167,17 +175,21 @@ struct PrepParams {
   const float* wtot;    // device scalar sum_j w_j (with cw)
   float4* coef;
   float* gval;          // device scalar g (written by the denominator pass)
-  float* bval;          // device scalar B = g eps / V
+  float* bval;          // device scalar B = g' eps / V
+  float gscale;         // > 0: g' = gscale replaces g in B and the coefficients (f16 band)
   int* err;
 };
 
 struct ColsumParams {
-  const uint16_t* band;  // bf16 [N][ld]
+  const uint16_t* band;  // bf16 or f16 [N][ld]
   int N, ld, cols;
   int row_chunks;
   float* partial;        // [row_chunks][cols]
   float* out;            // [cols]
   int accumulate;        // add to out instead of overwriting
+  int f16;               // the band holds f16 values
+  const float* scale;    // null, or column sums are multiplied by *scale * scale_mul
+  float scale_mul;
 };
 
 // Rows of one GEMM output tile (a CTA pair: 2 x 128).
@@ -191,8 +203,9 @@ int forward_max_units();
 
 // ext: the extended epilogue (bias, softcap, class weights, argmax); else the plain one.
 // w_vd: W is stored [V, D] (B is K-major); else [D, V] (B is MN-major).
+// f16: X and W are f16 (else bf16).
 cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const FwdParams& p, bool ext,
-                                bool w_vd, cudaStream_t stream);
+                                bool w_vd, bool f16, cudaStream_t stream);
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream);
 // g and B from the mean denominator over all rows (one block).
 cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream);
@@ -207,12 +220,14 @@ cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream);
 // gradient and dX GEMMs. The dW GEMM takes both operands MN-major in either layout (the
 // caller swaps them for a [V, D] dW).
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, cudaStream_t stream);
+                             const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, bool f16,
+                             cudaStream_t stream);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, bool f16, cudaStream_t stream);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, cudaStream_t stream);
-cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, int num_sms, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, bool w_vd, bool f16, cudaStream_t stream);
+// fp32 -> bf16 (or f16) of n elements, n a multiple of 4.
+cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream);
 
 constexpr int kFinalizeThreads = 256;
 

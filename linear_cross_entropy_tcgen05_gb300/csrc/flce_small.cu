@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kPrepThreads) flce_denominator_kernel(const Pr
       float g = *p.grad_out;
       if (p.reduction == 0) g = c != 0.0 ? float(double(g) / c) : 0.f;
       *p.gval = g;
-      *p.bval = g * p.eps / float(p.V);
+      *p.bval = (p.gscale > 0.f ? p.gscale : g) * p.eps / float(p.V);
     }
   }
 }
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kPrepThreads) flce_denominator_kernel(const Pr
 __global__ void __launch_bounds__(256) flce_coef_kernel(const PrepParams p, int n_rows) {
   const int i = int(blockIdx.x) * 256 + int(threadIdx.x);
   if (i >= n_rows) return;
-  const float g = *p.gval;
+  const float g = p.gscale > 0.f ? p.gscale : *p.gval;
   const float wtot = p.cw != nullptr ? *p.wtot : float(p.V);
   const int y = p.targets[i];
   float4 cf;
@@ -244,9 +244,10 @@ __global__ void __launch_bounds__(256) flce_colsum_partial_kernel(const ColsumPa
   const int r0 = int(blockIdx.y) * rows_per;
   const int r1 = min(p.N, r0 + rows_per);
   float s = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const uint16_t h = p.band[size_t(r) * p.ld + col];
-    s += __uint_as_float(uint32_t(h) << 16);
+  if (p.f16) {
+    for (int r = r0; r < r1; ++r) s += __half2float(__ushort_as_half(p.band[size_t(r) * p.ld + col]));
+  } else {
+    for (int r = r0; r < r1; ++r) s += __uint_as_float(uint32_t(p.band[size_t(r) * p.ld + col]) << 16);
   }
   p.partial[size_t(blockIdx.y) * p.cols + col] = s;
 }
@@ -254,17 +255,25 @@ __global__ void __launch_bounds__(256) flce_colsum_partial_kernel(const ColsumPa
 __global__ void __launch_bounds__(256) flce_colsum_final_kernel(const ColsumParams p) {
   const int col = int(blockIdx.x) * 256 + int(threadIdx.x);
   if (col >= p.cols) return;
-  float s = p.accumulate ? p.out[col] : 0.f;
+  float s = 0.f;
   for (int c = 0; c < p.row_chunks; ++c) s += p.partial[size_t(c) * p.cols + col];
-  p.out[col] = s;
+  if (p.scale != nullptr) s *= *p.scale * p.scale_mul;
+  p.out[col] = p.accumulate ? p.out[col] + s : s;
 }
 
-__global__ void flce_cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+template <bool F16>
+__global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
     const float4 v = src[i];
-    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    if constexpr (F16) {
+      const __half2 a = __floats2half2_rn(v.x, v.y);
+      const __half2 b = __floats2half2_rn(v.z, v.w);
+      dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    } else {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+      dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
   }
 }
 
@@ -303,14 +312,18 @@ cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, int num_sms, cudaStream_t stream) {
+cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream) {
   const size_t n4 = n / 4;
   size_t blocks = (n4 + 255) / 256;
   const size_t cap = size_t(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
-  flce_cast_bf16_kernel<<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
-                                                              reinterpret_cast<uint2*>(dst), n4);
+  if (f16)
+    flce_cast_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                                 reinterpret_cast<uint2*>(dst), n4);
+  else
+    flce_cast_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                                  reinterpret_cast<uint2*>(dst), n4);
   return cudaGetLastError();
 }
 

@@ -157,6 +157,27 @@ def test_python_wrapper_checks_the_weight_layout_shape():
         flce.linear_cross_entropy(X, Wvd, y, weight_layout="vd")  # shapes fine, CPU tensors refused
 
 
+def test_python_wrapper_names_the_input_dtype():
+    """The library cannot see an element type: the wrappers refuse f16 tensors unless the
+    options say f16, and bf16 ones if they do (checked before any library call)."""
+    X16 = torch.zeros(4, 8, dtype=torch.float16)
+    W16 = torch.zeros(8, 16, dtype=torch.float16)
+    y = torch.zeros(4, dtype=torch.int32)
+    out = torch.zeros(4)
+    with pytest.raises(TypeError, match="input_dtype"):
+        flce.flce_forward(X16, W16, y, out, out, out)
+    with pytest.raises(TypeError, match="input_dtype"):
+        flce.flce_forward_ex(X16, W16, y, out, out, out, options=flce.make_options())
+    with pytest.raises(TypeError, match="input_dtype"):
+        flce.flce_backward_ex(X16.bfloat16(), W16, y, out, out, out, out, out,
+                              options=flce.make_options(input_dtype="f16"))
+    assert flce.make_options(input_dtype=torch.float16).input_dtype == 1
+    with pytest.raises(TypeError, match="both"):
+        flce.linear_cross_entropy(X16, W16.bfloat16(), y)
+    with pytest.raises(ValueError, match="CUDA"):
+        flce.linear_cross_entropy(X16, W16, y)                     # f16 accepted, CPU tensors refused
+
+
 def test_python_wrapper_validates_dtypes():
     X = torch.zeros(4, 8, dtype=torch.float32)
     W = torch.zeros(8, 16, dtype=torch.bfloat16)
@@ -194,6 +215,7 @@ def test_option_checks(lib):
     assert _bwd_ex(lib, _opts(dX_f32=0xA0008)) == 2         # fp32 dX needs 16-byte alignment
     assert _fwd_ex(lib, _opts(weight_layout=2)) == 1        # not a flce_weight_layout
     assert _bwd_ex(lib, _opts(weight_layout=-1)) == 1
+    assert _fwd_ex(lib, _opts(input_dtype=2)) == 1          # not a flce_input_dtype
     assert lib.flce_combine_shards(0x10000, 0, 0x30000, 256, 1024, -100, 0.0, 0.0, 0, 0x40000, 0x50000,
                                    0x60000, 1 << 20, None) == 1   # K >= 1
     assert lib.flce_shard_stats(0x10000, 0x20000, 0x30000, 256, 128, 1024, -8, -100, 0x40000, 0x60000,

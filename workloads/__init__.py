@@ -107,11 +107,12 @@ def _fill_normal(out: np.ndarray, seed_seq: np.random.SeedSequence, scale: float
         list(ex.map(work, range(nblocks)))
 
 
-def normal_bf16(shape, seed_seq: np.random.SeedSequence, scale: float = 1.0) -> torch.Tensor:
-    """A bf16 tensor of N(0, scale^2) draws, rounded to nearest even."""
+def normal_bf16(shape, seed_seq: np.random.SeedSequence, scale: float = 1.0,
+                dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """A bf16 (or f16) tensor of N(0, scale^2) draws, rounded to nearest even."""
     buf = np.empty(int(np.prod(shape)), dtype=np.float32)
     _fill_normal(buf, seed_seq, scale)
-    return torch.from_numpy(buf).view(*shape).to(torch.bfloat16)
+    return torch.from_numpy(buf).view(*shape).to(dtype)
 
 
 def _zipf_ranks(g: np.random.Generator, n: int, V: int, s: float) -> np.ndarray:
@@ -140,16 +141,17 @@ def make_targets(wl: Workload, seed_seq: np.random.SeedSequence) -> torch.Tensor
     return torch.from_numpy(y.astype(np.int32))
 
 
-def make_inputs(wl: Workload, seed: int | None = None):
-    """Draw (X bf16 [N,D], W bf16 [D,V], targets int32 [N]) on the CPU.
+def make_inputs(wl: Workload, seed: int | None = None, dtype: torch.dtype = torch.bfloat16):
+    """Draw (X [N,D], W [D,V], targets int32 [N]) on the CPU; X and W in bf16 (or f16,
+    rounded from the same fp32 draws).
 
     Draw order: X, W, targets (with the ignore mask). ``seed`` overrides the
     workload's own seed.
     """
     root = np.random.SeedSequence(wl.seed if seed is None else seed)
     sx, sw, sy = root.spawn(3)
-    X = normal_bf16((wl.N, wl.D), sx, 1.0)
-    W = normal_bf16((wl.D, wl.V), sw, 1.0 / math.sqrt(wl.D))
+    X = normal_bf16((wl.N, wl.D), sx, 1.0, dtype)
+    W = normal_bf16((wl.D, wl.V), sw, 1.0 / math.sqrt(wl.D), dtype)
     y = make_targets(wl, sy)
     return X, W, y
 

@@ -34,7 +34,11 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <atomic>
+#include <mutex>
+#include <set>
 #include <type_traits>
+#include <utility>
 
 #include "flce_internal.h"
 #include "sm103_ptx.cuh"
@@ -939,9 +943,23 @@ constexpr int kMC = FLCE_PAIRS_PER_CLUSTER;  // pairs sharing B through TMA mult
 constexpr int kFwdStages = 7;    // 7 x 32 KB
 constexpr int kWalkStages = 6;   // 6 x 32 KB + 2 x 16 KB epilogue boxes
 
+// Opt a kernel in to its dynamic shared memory, once per kernel and device: the launch
+// path then makes no attribute calls, so a warmed-up call sequence can be captured into
+// a CUDA graph.
+std::mutex g_prepared_mu;
+std::set<std::pair<const void*, int>> g_prepared;
+
 template <class Kern>
 cudaError_t prepare(Kern kernel, size_t smem) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+  std::lock_guard<std::mutex> lock(g_prepared_mu);
+  if (g_prepared.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e == cudaSuccess) g_prepared.insert(key);
+  return e;
 }
 
 cudaLaunchConfig_t make_config(int grid, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
@@ -960,12 +978,14 @@ cudaLaunchConfig_t make_config(int grid, size_t smem, cudaStream_t stream, cudaL
 }
 
 // Clusters that can be resident at once (cached per device and kernel kind).
+std::atomic<int> g_max_clusters[64][4];
+
 template <class Kern>
 int max_clusters(Kern kernel, size_t smem, int slot) {
-  static int cache[64][4];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cache[dev][slot] > 0) return cache[dev][slot];
+  const int cached = g_max_clusters[dev][slot].load(std::memory_order_relaxed);
+  if (cached > 0) return cached;
   if (prepare(kernel, smem) != cudaSuccess) return 0;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -976,7 +996,7 @@ int max_clusters(Kern kernel, size_t smem, int slot) {
     cudaGetLastError();
     n = sms / (kCG * kMC);
   }
-  cache[dev][slot] = n;
+  g_max_clusters[dev][slot].store(n, std::memory_order_relaxed);
   return n;
 }
 

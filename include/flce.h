@@ -212,6 +212,14 @@ flce_status flce_shard_stats(const void* X, const void* W, const int32_t* target
                              int64_t N, int64_t D, int64_t V, int64_t v_offset, int32_t ignore_index,
                              float* stats, void* workspace, size_t ws_bytes, struct CUstream_st* stream);
 
+/* flce_shard_stats for W stored [V, D] (the shard is rows [v_offset, v_offset + V) of the
+ * full weight) or f16 inputs: opt may set weight_layout and input_dtype, every other
+ * field must be zero (FLCE_ERR_INVALID_ARG otherwise). NULL behaves like flce_shard_stats. */
+flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* targets,
+                                int64_t N, int64_t D, int64_t V, int64_t v_offset, int32_t ignore_index,
+                                const flce_options* opt, float* stats, void* workspace, size_t ws_bytes,
+                                struct CUstream_st* stream);
+
 /* Combine K shards' stats (device fp32 [K][4][N], shard order irrelevant) into the
  * full-vocabulary lse [N] and the loss, as flce_forward would for the whole
  * vocabulary of v_total classes. Workspace: flce_workspace_size(N, 8, 8, 0). */

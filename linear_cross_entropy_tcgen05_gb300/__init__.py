@@ -42,7 +42,7 @@ STATUS = {
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
                     "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards",
-                    "flce_last_error_detail")
+                    "flce_last_error_detail", "flce_shard_stats_ex")
 
 
 class FlceOptions(ctypes.Structure):
@@ -137,6 +137,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_forward_backward.restype = ctypes.c_int
     lib.flce_shard_stats.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, sz, vp]
     lib.flce_shard_stats.restype = ctypes.c_int
+    lib.flce_shard_stats_ex.argtypes = [vp, vp, vp, i64, i64, i64, i64, i32, vp, vp, vp, sz, vp]
+    lib.flce_shard_stats_ex.restype = ctypes.c_int
     lib.flce_combine_shards.argtypes = [vp, i32, vp, i64, i64, i32, f32, f32, ctypes.c_int, vp, vp, vp, sz, vp]
     lib.flce_combine_shards.restype = ctypes.c_int
     if path is None:
@@ -275,11 +277,17 @@ def flce_forward_backward(X, W, targets, grad_out, loss, lse, dX, dW, workspace,
 
 
 def flce_shard_stats(X, W_shard, targets, v_offset: int, stats, workspace, ignore_index: int = -100, stream=None,
-                     raise_on_error: bool = True) -> int:
-    """Call flce_shard_stats: stats is a device fp32 [4, N] tensor."""
-    st = load_library().flce_shard_stats(
-        _ptr(X), _ptr(W_shard), _ptr(targets), X.shape[0], X.shape[1], W_shard.shape[1], int(v_offset),
-        int(ignore_index), _ptr(stats), _ptr(workspace), _nbytes(workspace), _stream(stream))
+                     raise_on_error: bool = True, options: FlceOptions | None = None) -> int:
+    """Call flce_shard_stats (or flce_shard_stats_ex with ``options``: weight layout and
+    input dtype only): stats is a device fp32 [4, N] tensor."""
+    _check_dtype(X, options)
+    args = (_ptr(X), _ptr(W_shard), _ptr(targets), X.shape[0], X.shape[1], _vocab(W_shard, options), int(v_offset),
+            int(ignore_index))
+    tail = (_ptr(stats), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    if options is None:
+        st = load_library().flce_shard_stats(*args, *tail)
+    else:
+        st = load_library().flce_shard_stats_ex(*args, ctypes.byref(options), *tail)
     if raise_on_error:
         _check(st, "flce_shard_stats")
     return st

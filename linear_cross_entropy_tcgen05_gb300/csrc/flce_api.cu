@@ -695,6 +695,21 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
 flce_status flce_shard_stats(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
                              int64_t v_offset, int32_t ignore_index, float* stats, void* workspace, size_t ws_bytes,
                              struct CUstream_st* stream) {
+  return flce_shard_stats_ex(X, W, targets, N, D, V, v_offset, ignore_index, nullptr, stats, workspace, ws_bytes,
+                             stream);
+}
+
+flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D,
+                                int64_t V, int64_t v_offset, int32_t ignore_index, const flce_options* opt,
+                                float* stats, void* workspace, size_t ws_bytes, struct CUstream_st* stream) {
+  if (opt) {
+    // only the storage options apply to shard statistics
+    if (opt->softcap != 0.f || opt->bias || opt->class_weight || opt->predicted || opt->accuracy || opt->dbias ||
+        opt->dX_f32 || opt->v_offset != 0 || opt->v_total != 0 || opt->row_band != 0)
+      return FLCE_ERR_INVALID_ARG;
+    if (opt->weight_layout != FLCE_WEIGHT_DV && opt->weight_layout != FLCE_WEIGHT_VD) return FLCE_ERR_INVALID_ARG;
+    if (opt->input_dtype != FLCE_INPUT_BF16 && opt->input_dtype != FLCE_INPUT_F16) return FLCE_ERR_INVALID_ARG;
+  }
   flce_status st = check_common(X, W, targets, N, D, V, 0.f, 0.f, 0, workspace);
   if (st != FLCE_OK) return st;
   if (!stats) return FLCE_ERR_INVALID_ARG;
@@ -709,7 +724,7 @@ flce_status flce_shard_stats(const void* X, const void* W, const int32_t* target
     note_error("forward_max_units", "no resident cluster");
     return FLCE_ERR_CUDA;
   }
-  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, false, false};
+  const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, opt_w_vd(opt), opt_f16(opt)};
   return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
                      static_cast<uint8_t*>(workspace), true, units, reinterpret_cast<cudaStream_t>(stream));
 }

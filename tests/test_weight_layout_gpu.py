@@ -135,3 +135,48 @@ def test_vd_layout_through_autograd(gpu_lib):
     assert rel_fro(Xa.grad.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
     # the autograd path returns dW in W's dtype (bf16): compare at bf16 resolution
     assert rel_fro(Wa.grad.float().cpu().numpy().T, ref_dW) <= 1e-2
+
+
+def test_vd_f16_shards_end_to_end(gpu_lib):
+    """Vocabulary shards of an f16 [V, D] weight: statistics, combination and backward."""
+    from workloads import make_inputs as mk
+    wl = custom("vd_f16_shard", 640, 136, 4104, seed=45, ignore_frac=0.1, label_smoothing=0.1)
+    X, W, y = mk(wl, dtype=torch.float16)
+    N, D, V = wl.N, wl.D, wl.V
+    Xd, yd = X.to(DEV), y.to(DEV)
+    cuts = [0, 1544, 4104]
+    K = len(cuts) - 1
+    stats = torch.empty(K, 4, N, device=DEV)
+    opt = flce.make_options(weight_layout="vd", input_dtype="f16")
+    shards = []
+    for k, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        Wk = W[:, a:b].t().contiguous().to(DEV)
+        shards.append((a, Wk))
+        ws = _ws(N, D, b - a, 0)
+        flce.flce_shard_stats(Xd, Wk, yd, a, stats[k], ws, options=opt)
+        assert flce.flce_check_device_error(ws) == 0
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    wsc = _ws(N, 8, 8, 0)
+    flce.flce_combine_shards(stats, yd, V, loss, lse, wsc, label_smoothing=0.1)
+    assert flce.flce_check_device_error(wsc) == 0
+    g = torch.ones(1, device=DEV)
+    dX = torch.zeros(N, D, device=DEV)
+    dW = torch.empty(V, D, device=DEV)
+    for a, Wk in shards:
+        Vk = Wk.shape[0]
+        part = torch.empty(N, D, device=DEV)
+        dWk = torch.empty(Vk, D, device=DEV)
+        ws = _ws(N, D, Vk, 1)
+        flce.flce_backward_ex(Xd, Wk, yd, lse, g, None, dWk, ws, label_smoothing=0.1,
+                              options=flce.make_options(dX_f32=part, v_offset=a, v_total=V, weight_layout="vd",
+                                                        input_dtype="f16"))
+        assert flce.flce_check_device_error(ws) == 0
+        dX += part
+        dW[a:a + Vk] = dWk
+    torch.cuda.synchronize()
+    ref_loss, ref_lse, ref_dX, ref_dW = oracle.forward_backward(X, W, y, label_smoothing=0.1)
+    valid = y.numpy() != IGNORE_INDEX
+    assert abs(loss.item() - ref_loss) <= TOL_LOSS_REL * abs(ref_loss)
+    assert np.max(np.abs(lse.cpu().double().numpy()[valid] - ref_lse[valid])) <= TOL_LSE_ABS
+    assert rel_fro(dX.cpu().numpy(), ref_dX) <= 5e-3
+    assert rel_fro(dW.cpu().numpy().T, ref_dW) <= TOL_DW_REL

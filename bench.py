@@ -269,6 +269,7 @@ def run_ours(args, wl, world, rank, local):
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(dev)
+    launches_before = flce.flce_kernel_launches()
     with ClockSampler(local) as clk:
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
@@ -280,6 +281,7 @@ def run_ours(args, wl, world, rank, local):
             bwd()
             ev[i][2].record(stream)
         end.record(stream)
+        launches_timed = flce.flce_kernel_launches() - launches_before
         torch.cuda.synchronize(dev)
         barrier(world)
     total_ms = start.elapsed_time(end)
@@ -295,7 +297,7 @@ def run_ours(args, wl, world, rank, local):
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
     e2e_value, e2e_ms, h2d, d2h = run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd)
     return finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc,
-                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk)
+                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed)
 
 
 def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
@@ -372,7 +374,7 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
 
 
 def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
-           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk):
+           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -423,7 +425,10 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": launches * args.steps,
+        # counted by the library (flce_kernel_launches) over the timed region; the band
+        # schedule predicts launches_per_step x steps
+        "gpu_launches": launches_timed,
+        "gpu_launches_per_step_expected": launches,
         "clocks": clk.summary(),
     }
     print(json.dumps(out), flush=True)

@@ -247,6 +247,11 @@ int flce_version(void);
  * pages have no counterpart. */
 const char* flce_last_error_detail(void);
 
+/* Number of kernels this library has launched in the process so far, over every thread
+ * and device (a relaxed atomic counter; each launch counts itself when it is issued).
+ * For profiling and launch accounting; the pages have no counterpart. */
+unsigned long long flce_kernel_launches(void);
+
 /* Forward pass without a workspace, for callers that cannot allocate device memory
  * (code inside an allocator or memory-pool callback, runtimes that give a fixed
  * device arena and forbid further allocation). The source pages have no

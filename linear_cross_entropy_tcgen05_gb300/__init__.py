@@ -25,7 +25,7 @@ __all__ = [
     "flce_check_device_error", "flce_status_string", "flce_version", "linear_cross_entropy",
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
-    "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail",
+    "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail", "flce_kernel_launches",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +42,7 @@ STATUS = {
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
                     "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards",
-                    "flce_last_error_detail", "flce_shard_stats_ex")
+                    "flce_last_error_detail", "flce_shard_stats_ex", "flce_kernel_launches")
 
 
 class FlceOptions(ctypes.Structure):
@@ -126,6 +126,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_version.restype = ctypes.c_int
     lib.flce_last_error_detail.argtypes = []
     lib.flce_last_error_detail.restype = ctypes.c_char_p
+    lib.flce_kernel_launches.argtypes = []
+    lib.flce_kernel_launches.restype = ctypes.c_ulonglong
     op = ctypes.POINTER(FlceOptions)
     lib.flce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp, sz, vp]
     lib.flce_forward_ex.restype = ctypes.c_int
@@ -152,6 +154,11 @@ def flce_status_string(status: int) -> str:
 
 def flce_version() -> int:
     return int(load_library().flce_version())
+
+
+def flce_kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().flce_kernel_launches())
 
 
 def flce_last_error_detail() -> str:

@@ -264,6 +264,8 @@ int flce_version(void) { return 100; }
 
 const char* flce_last_error_detail(void) { return g_detail; }
 
+unsigned long long flce_kernel_launches(void) { return launches_so_far(); }
+
 const char* flce_status_string(flce_status st) {
   switch (st) {
     case FLCE_OK: return "FLCE_OK";

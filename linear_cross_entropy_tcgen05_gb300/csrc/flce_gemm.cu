@@ -1,20 +1,22 @@
 // flce_gemm.cu -- the tensor-core kernels of fused linear cross-entropy on sm_103a.
 //
 // All four GEMMs share one warp-specialised, persistent skeleton, run by a pair of
-// CTAs on two SMs (a cluster of 2, tcgen05 cta_group::2) that together own a 256 x 256
-// output tile; each CTA holds 128 rows of it:
+// CTAs on two SMs (tcgen05 cta_group::2) that together own a 256 x 256 output tile;
+// each CTA holds 128 rows of it. A cluster holds MC such pairs (two by default) whose
+// tiles share the B operand: pair 0 loads each B block once and multicasts it into
+// every pair of the cluster.
 //   warp 0      : TMA producer. One lane streams this CTA's 128 rows of A and its half
 //                 (128 columns) of B, 64-deep K blocks, 128-byte swizzled, into a
-//                 multi-stage ring; the completions land on the leader CTA's barrier.
+//                 multi-stage ring; the completions land on the pair leader's barrier.
 //   warp 1      : TMEM owner (both CTAs allocate 512 columns together: two 128x256
 //                 fp32 accumulators per CTA). In the leader CTA one lane issues
 //                 tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads both CTAs'
-//                 shared memory, and multicasts each stage's completion to both
-//                 producers and each finished accumulator to both epilogues.
+//                 shared memory, and multicasts each stage's completion to the producers
+//                 of the whole cluster and each finished accumulator to both epilogues.
 //   warps 2..5  : epilogue. Thread r owns TMEM lane r = output row r of its CTA, so every
 //                 per-row reduction is thread-local; the epilogue of one tile overlaps
 //                 the MMAs of the next.
-// A single-CTA variant (CG = 1, M = 128) is kept for comparison.
+// The skeleton also compiles for a single CTA (CG = 1, M = 128) and for MC = 1.
 //
 // The epilogues:
 //   forward   : online softmax over the tile's vocabulary columns (running max m, sum
@@ -1026,6 +1028,7 @@ cudaError_t launch_walk(Kern kernel, const CUtensorMap& tmA, const CUtensorMap& 
   const int clusters = w.total_tiles < maxc ? w.total_tiles : maxc;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config(clusters * kCG * kMC, kWalkSmem, stream, attr);
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, w, g, s);
 }
 
@@ -1067,6 +1070,7 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config(p.gN * p.S * kCG * kMC, kFwdSmem, stream, attr);
+  count_launch();
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 

@@ -15,7 +15,7 @@ constexpr int FLCE_DEVERR_BAD_TARGET = 1;
 constexpr int FLCE_DEVERR_TIMEOUT = 2;
 
 // Output tiles of the tensor-core GEMMs: 128 rows per CTA (TMEM lanes) x 256 columns,
-// a CTA pair (cluster of 2) owning 256 x 256; K staged 64 bf16 (128 bytes, one
+// a CTA pair owning 256 x 256; K staged 64 16-bit elements (128 bytes, one
 // 128B-swizzle row) at a time.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
@@ -215,7 +215,7 @@ cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream);
 cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream);
 // Column sums of a bf16 band, fixed order (two kernels).
 cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream);
-// The walk GEMMs size their own grids: min(tiles, resident CTA pairs) clusters of 2.
+// The walk GEMMs size their own grids: min(tile groups, resident clusters) clusters.
 // w_vd as in launch_forward_gemm: it sets the major-ness of W, the B operand of the
 // gradient and dX GEMMs. The dW GEMM takes both operands MN-major in either layout (the
 // caller swaps them for a [V, D] dW).
@@ -230,5 +230,9 @@ cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream);
 
 constexpr int kFinalizeThreads = 256;
+
+// Kernels this library has launched in the process (every launch site counts itself).
+void count_launch();
+unsigned long long launches_so_far();
 
 }  // namespace flce

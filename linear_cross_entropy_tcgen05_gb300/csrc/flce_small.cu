@@ -2,6 +2,8 @@
 // cross-entropy: the forward finalize (combine the vocabulary splits into lse, form the
 // row losses, reduce them in a fixed order), the backward prep (valid-row count and
 // per-row gradient coefficients) and the fp32 -> bf16 cast of dX.
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -280,35 +282,50 @@ __global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restri
 // ---------------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------------
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+unsigned long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
+
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream) {
   flce_finalize_rows_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(p);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.mode == FIN_SHARD_STATS || (p.reduction == 2 && p.accuracy == nullptr)) return e;
   flce_finalize_loss_kernel<<<1, kFinalizeThreads, 0, stream>>>(p, blocks);
+  count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream) {
   flce_denominator_kernel<<<1, kPrepThreads, 0, stream>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream) {
   flce_coef_kernel<<<unsigned((n_rows + 255) / 256), 256, 0, stream>>>(p, n_rows);
+  count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream) {
   flce_sum_kernel<<<1, 1024, 0, stream>>>(v, n, out);
+  count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream) {
   const dim3 grid(unsigned((p.cols + 255) / 256), unsigned(p.row_chunks));
   flce_colsum_partial_kernel<<<grid, 256, 0, stream>>>(p);
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   flce_colsum_final_kernel<<<unsigned((p.cols + 255) / 256), 256, 0, stream>>>(p);
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -324,6 +341,7 @@ cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, i
   else
     flce_cast_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
                                                                   reinterpret_cast<uint2*>(dst), n4);
+  count_launch();
   return cudaGetLastError();
 }
 

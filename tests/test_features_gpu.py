@@ -247,3 +247,24 @@ def test_row_band_backward_matches_the_oracle(gpu_lib, row_band, opts):
     st = flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, small, *common, raise_on_error=False,
                                options=flce.make_options(row_band=row_band))
     assert st == 4
+
+
+def test_launch_counter_matches_the_band_schedule(gpu_lib):
+    """flce_kernel_launches counts what the bench reports as gpu_launches; one forward
+    plus backward launches what the band schedule predicts."""
+    import bench
+    wl = custom("count", 1000, 136, 4104, seed=37, ignore_frac=0.1)
+    X, W, y, _, _ = _inputs(wl)
+    N, D, V = wl.N, wl.D, wl.V
+    Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
+    ws = _ws(N, D, V, 2)
+    loss, lse, g = torch.empty(1, device=DEV), torch.empty(N, device=DEV), torch.ones(1, device=DEV)
+    dX = torch.empty(N, D, dtype=torch.bfloat16, device=DEV)
+    dW = torch.empty(D, V, device=DEV)
+    before = flce.flce_kernel_launches()
+    flce.flce_forward(Xd, Wd, yd, loss, lse, ws)
+    flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws)
+    counted = flce.flce_kernel_launches() - before
+    assert flce.flce_check_device_error(ws) == 0
+    expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean")
+    assert bands == 2 and counted == expected

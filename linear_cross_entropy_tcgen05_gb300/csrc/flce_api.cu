@@ -354,14 +354,13 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
 
   // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;
-  const bool enc_w = pb.w_vd ? encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.D),
-                                         uint64_t(pb.V), uint64_t(pb.D), 64, uint32_t(gemm_b_rows_per_cta()))
-                             : encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.V),
-                                         uint64_t(pb.D), uint64_t(pb.V), 64, 64);
-  if (!encode_2d(&tmX, pb.dt16(), 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D),
-                 64, kBM) ||
-      !enc_w)
-    return FLCE_ERR_CUDA;
+  const bool enc_w =
+      pb.w_vd ? encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.D), uint64_t(pb.V), uint64_t(pb.D), 64,
+                          uint32_t(gemm_b_rows_per_cta()))
+              : encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64, 64);
+  const bool enc_x =
+      encode_2d(&tmX, pb.dt16(), 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64, kBM);
+  if (!enc_w || !enc_x) return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
   const float* cw = opt ? opt->class_weight : nullptr;

@@ -302,9 +302,10 @@ def run_ours(args, wl, world, rank, local):
 
 def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
     """End to end through the public API: every step copies X, W and targets from pinned
-    host memory to the device and loss, dX and dW back. Copies run on their own streams,
-    double-buffered, so step i's compute overlaps the input copy of step i+1 and the
-    result copy of step i-1 (what a training loop feeding this op would do)."""
+    host memory to the device and loss, dX and dW back. Copies run on their own streams
+    with three buffer sets, so step i's compute overlaps the input copy of step i+1 and the
+    result copy of step i-1, and a copy slowed by the shared host link has two steps of
+    slack before compute waits for it (what a training loop feeding this op would do)."""
     if args.no_e2e:
         return None, None, 0, 0
     import linear_cross_entropy_tcgen05_gb300 as flce
@@ -316,25 +317,24 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
     dW_h = torch.empty(D, V, dtype=torch.float32).pin_memory()
     h2d = Xh.numel() * 2 + Wh.numel() * 2 + yh.numel() * 4
     d2h = 4 + dX_h.numel() * 2 + dW_h.numel() * 4
-    # two buffer sets: set 0 reuses the resident buffers, set 1 is a second copy
-    bufs = [(Xd, Wd, yd, loss, dX, dW),
-            (torch.empty_like(Xd), torch.empty_like(Wd), torch.empty_like(yd), torch.empty_like(loss),
-             torch.empty_like(dX), torch.empty_like(dW))]
-    ws2 = [None, None]
+    # buffer sets: set 0 reuses the resident buffers, the others are copies
+    nbuf = 3
+    bufs = [(Xd, Wd, yd, loss, dX, dW)] + [
+        (torch.empty_like(Xd), torch.empty_like(Wd), torch.empty_like(yd), torch.empty_like(loss),
+         torch.empty_like(dX), torch.empty_like(dW)) for _ in range(nbuf - 1)]
     nbytes = max(flce.flce_workspace_size(N, D, V, 0), flce.flce_workspace_size(N, D, V, 1))
-    ws2[0] = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    ws2[1] = ws2[0]  # compute is serialised on one stream: one workspace suffices
+    ws_e2e = torch.empty(nbytes, dtype=torch.uint8, device=dev)  # compute is serialised on one stream
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     g = torch.ones(1, dtype=torch.float32, device=dev)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
-    inputs_free = [torch.cuda.Event(), torch.cuda.Event()]
-    inputs_ready = [torch.cuda.Event(), torch.cuda.Event()]
-    outputs_ready = [torch.cuda.Event(), torch.cuda.Event()]
-    outputs_free = [torch.cuda.Event(), torch.cuda.Event()]
+    inputs_free = [torch.cuda.Event() for _ in range(nbuf)]
+    inputs_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    outputs_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    outputs_free = [torch.cuda.Event() for _ in range(nbuf)]
     opts = (args._wl.ignore_index, args._wl.label_smoothing, args._wl.zloss_scale, args._wl.reduction)
     steps = max(1, args.steps)
-    warm = 2
+    warm = nbuf
     for ev in inputs_free + outputs_free:
         ev.record(stream)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -344,7 +344,7 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
             torch.cuda.synchronize(dev)
             barrier(world)
             t0.record(stream)
-        b = it % 2
+        b = it % nbuf
         Xb, Wb, yb, lb, dXb, dWb = bufs[b]
         with torch.cuda.stream(s_in):
             s_in.wait_event(inputs_free[b])
@@ -354,8 +354,8 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
             inputs_ready[b].record(s_in)
         stream.wait_event(inputs_ready[b])
         stream.wait_event(outputs_free[b])
-        flce.flce_forward(Xb, Wb, yb, lb, lse, ws2[b], *opts, stream=stream)
-        flce.flce_backward(Xb, Wb, yb, lse, g, dXb, dWb, ws2[b], *opts, stream=stream)
+        flce.flce_forward(Xb, Wb, yb, lb, lse, ws_e2e, *opts, stream=stream)
+        flce.flce_backward(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts, stream=stream)
         inputs_free[b].record(stream)
         outputs_ready[b].record(stream)
         with torch.cuda.stream(s_out):

@@ -47,3 +47,19 @@ def test_launch_count_matches_the_band_schedule():
     import bench
     total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean")
     assert (bands, vc) == (16, 8192) and total == 3 + 2 + 3 * 16 + 1
+
+
+def test_clock_record_decides_a_remeasurement():
+    """Thermal or hardware slowdown, or clocks held far below maximum with no reason,
+    make the bench measure once more; the power cap alone does not."""
+    import bench
+    c = bench.ClockSampler(0)
+    row = "0, {mhz}, 2070, 1300, 0x0, {hw}, Not Active, Not Active, {cap}"
+    c.lines = [row.format(mhz=1600, hw="Not Active", cap="Active")] * 3
+    assert c.summary()["reasons"] == ["sw_power_cap"] and not c.throttled()
+    c.lines = [row.format(mhz=1600, hw="Active", cap="Active")] * 3
+    assert c.throttled()
+    c.lines = [row.format(mhz=900, hw="Not Active", cap="Not Active")] * 3
+    assert c.throttled()
+    c.lines = []
+    assert c.summary()["samples"] == 0 and not c.throttled()

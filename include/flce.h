@@ -252,6 +252,14 @@ const char* flce_last_error_detail(void);
  * For profiling and launch accounting; the pages have no counterpart. */
 unsigned long long flce_kernel_launches(void);
 
+/* Self-test of failure detection: launches one small kernel whose pipeline wait (the
+ * bounded mbarrier wait every GEMM uses) waits for an arrival that never comes, gives up
+ * after the wait limit (2 s) and records FLCE_DEVERR_TIMEOUT in the workspace header
+ * instead of hanging. Asynchronous like every call; flce_check_device_error then returns
+ * FLCE_ERR_TIMEOUT, and the context stays usable. workspace: at least 256 bytes.
+ * Diagnostics only; the pages have no counterpart. */
+flce_status flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, struct CUstream_st* stream);
+
 /* Forward pass without a workspace, for callers that cannot allocate device memory
  * (code inside an allocator or memory-pool callback, runtimes that give a fixed
  * device arena and forbid further allocation). The source pages have no

@@ -266,6 +266,19 @@ const char* flce_last_error_detail(void) { return g_detail; }
 
 unsigned long long flce_kernel_launches(void) { return launches_so_far(); }
 
+flce_status flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, struct CUstream_st* stream_) {
+  if (!workspace) return FLCE_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return FLCE_ERR_ALIGNMENT;
+  if (ws_bytes < kHeaderBytes) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  flce_status st = current_device(&sms);
+  if (st != FLCE_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  FLCE_CUDA_CHECK(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
+  FLCE_CUDA_CHECK(launch_wait_selftest(reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kHdrErr), stream));
+  return FLCE_OK;
+}
+
 const char* flce_status_string(flce_status st) {
   switch (st) {
     case FLCE_OK: return "FLCE_OK";

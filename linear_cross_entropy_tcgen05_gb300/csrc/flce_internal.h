@@ -211,6 +211,8 @@ cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t st
 cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream);
 // Per-row gradient coefficients of rows [0, n_rows) of p.targets / p.lse into p.coef.
 cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream);
+// One block whose pipeline wait times out on purpose (bounded): sets the timeout bit.
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 // out[0] = sum of v[0..n) in a fixed order (one block).
 cudaError_t launch_sum(const float* v, int n, float* out, cudaStream_t stream);
 // Column sums of a bf16 band, fixed order (two kernels).

@@ -8,6 +8,7 @@
 #include <math_constants.h>
 
 #include "flce_internal.h"
+#include "sm103_ptx.cuh"
 #include "vec_split.h"
 
 namespace flce {
@@ -279,6 +280,24 @@ __global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restri
   }
 }
 
+// Self-test of the bounded pipeline wait: two threads wait on an mbarrier that nothing
+// arrives on, with the wait the GEMMs use. One gives up after the time limit and raises
+// the abort flag and FLCE_DEVERR_TIMEOUT; the other returns on the flag (or its own
+// limit). Nothing else runs: no copies, no tensor memory, no cluster.
+__global__ void __launch_bounds__(64) flce_wait_selftest_kernel(int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtx w{&abort_flag, err};
+  if (threadIdx.x == 0 || threadIdx.x == 32) mbar_wait(&bar, 0, w);
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------------
@@ -308,6 +327,12 @@ cudaError_t launch_denominator(const PrepParams& p, cudaStream_t stream) {
 
 cudaError_t launch_coef(const PrepParams& p, int n_rows, cudaStream_t stream) {
   flce_coef_kernel<<<unsigned((n_rows + 255) / 256), 256, 0, stream>>>(p, n_rows);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream) {
+  flce_wait_selftest_kernel<<<1, 64, 0, stream>>>(err);
   count_launch();
   return cudaGetLastError();
 }

@@ -135,6 +135,9 @@ def test_backward_argument_checks(lib):
 def test_refuses_without_a_supported_device(lib):
     assert _fwd(lib) == 3
     assert _bwd(lib) == 3
+    assert lib.flce_selftest_wait_timeout(0x60000, 4096, None) == 3
+    assert lib.flce_selftest_wait_timeout(None, 4096, None) == 1
+    assert lib.flce_selftest_wait_timeout(0x60000, 16, None) == 4
 
 
 def test_options_struct_matches_the_header():

@@ -36,18 +36,20 @@
  *
  * Data layout (all row-major, contiguous, device memory):
  *   X        bf16  [N, D]      row stride D elements
- *   W        bf16  [D, V]      row stride V elements (note: not nn.Linear's [V, D])
+ *   W        bf16  [D, V]      row stride V elements (nn.Linear's [V, D] and f16 inputs:
+ *                              flce_options.weight_layout and .input_dtype)
  *   targets  int32 [N]
  *   lse      fp32  [N]
  *   loss     fp32  [1] (MEAN, SUM) or [N] (NONE)
- *   dX       bf16  [N, D]
- *   dW       fp32  [D, V]
+ *   dX       bf16  [N, D]      (the type of X)
+ *   dW       fp32  [D, V]      (the layout of W)
  *
  * Ownership and execution: the caller owns every buffer, including the
  * workspace; the library never allocates or frees memory. All calls are
  * asynchronous on `stream` and never synchronise, except
  * flce_check_device_error. The library keeps no state between calls other than
- * per-device launch attributes; separate workspaces make calls independent.
+ * per-device launch attributes, a launch counter and a per-thread error detail;
+ * separate workspaces make calls independent.
  *
  * Errors: host-side argument checks return a status synchronously and launch
  * nothing. Conditions found on the device (a target outside [0, V) that is not
@@ -92,9 +94,9 @@ typedef enum {
 
 /* Bytes of workspace that flce_forward (for_backward == 0), flce_backward
  * (for_backward == 1) or flce_forward_backward (for_backward == 2) needs for this
- * shape. Returns 0 for invalid sizes. The backward workspace holds a bf16 gradient
- * band of N x Vc columns (Vc < V, a multiple of 256) and an fp32 [N, D] dX
- * accumulator; no buffer has N x V elements. */
+ * shape. Returns 0 for invalid sizes. The backward workspace holds a 16-bit gradient
+ * band of N x Vc columns (Vc a multiple of 512, at most 16384, and below V once V
+ * exceeds 512) and an fp32 [N, D] dX accumulator; no buffer has N x V elements. */
 size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward);
 
 /* Forward pass. [P1] "Definition and Forward Pass" and "Kernel Implementation"

@@ -23,7 +23,7 @@ def rel_fro(got, ref) -> float:
     return float(num / den) if den > 0 else float(num)
 
 
-class GpuRun:
+class CudaRun:
     """Device buffers and one forward (+ backward) of the CUDA path."""
 
     def __init__(self, X, W, y, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, GpuRun, rel_fro
+from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, CudaRun, rel_fro
 from workloads import custom, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -21,7 +21,7 @@ EXTREMES = [
 @pytest.mark.parametrize("name,wl", EXTREMES, ids=[c[0] for c in EXTREMES])
 def test_parity_at_extreme_shapes(gpu_lib, name, wl):
     X, W, y = make_inputs(wl)
-    run = GpuRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
     assert run.forward() == 0
     assert run.backward(1.0) == 0
     got = run.host()

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, GpuRun, rel_fro
+from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, CudaRun, rel_fro
 from workloads import IGNORE_INDEX, WORKLOADS, custom, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -26,7 +26,7 @@ CASES = [
 
 def _check(wl, grad_out=1.0):
     X, W, y = make_inputs(wl)
-    run = GpuRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
     assert run.forward() == 0
     assert run.backward(grad_out) == 0
     got = run.host()
@@ -56,7 +56,7 @@ def test_reduction_none_forward(gpu_lib):
     wl = custom("none", 600, 128, 3000, seed=14, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-3,
                 reduction="none")
     X, W, y = make_inputs(wl)
-    run = GpuRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "none")
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "none")
     assert run.forward() == 0
     got = run.host()
     ell, lse = oracle.forward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "none")
@@ -74,7 +74,7 @@ def test_reduction_none_forward(gpu_lib):
 def test_all_rows_ignored_mean_is_zero(gpu_lib):
     wl = custom("allign", 200, 64, 512, seed=15, ignore_frac=1.0)
     X, W, y = make_inputs(wl)
-    run = GpuRun(X, W, y)
+    run = CudaRun(X, W, y)
     assert run.forward() == 0
     assert run.backward() == 0
     got = run.host()
@@ -87,7 +87,7 @@ def test_bad_target_sets_the_error_word_and_poisons_its_row(gpu_lib):
     X, W, y = make_inputs(wl)
     y[5] = wl.V + 3
     y[9] = -7
-    run = GpuRun(X, W, y, reduction="none")
+    run = CudaRun(X, W, y, reduction="none")
     assert run.forward() == 7  # FLCE_ERR_BAD_TARGET
     got = run.host()
     assert np.isnan(got["loss"][5]) and np.isnan(got["loss"][9])
@@ -97,7 +97,7 @@ def test_bad_target_sets_the_error_word_and_poisons_its_row(gpu_lib):
     # the error word is cleared by reading it
     import linear_cross_entropy_tcgen05_gb300 as flce
     assert flce.flce_check_device_error(run.ws) == 0
-    run2 = GpuRun(X, W, y, reduction="sum")
+    run2 = CudaRun(X, W, y, reduction="sum")
     assert run2.forward() == 7
     assert run2.backward() == 7
     g = run2.host()
@@ -110,7 +110,7 @@ def test_bitwise_deterministic(gpu_lib):
     X, W, y = make_inputs(wl)
     outs = []
     for _ in range(2):
-        run = GpuRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+        run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
         assert run.forward() == 0 and run.backward() == 0
         outs.append(run.host())
     for k in ("loss", "lse", "dX", "dW"):
@@ -121,13 +121,13 @@ def test_ignored_rows_do_not_change_dw(gpu_lib):
     """Changing the hidden state of ignored rows leaves the loss and dW bit-identical."""
     wl = custom("ignx", 512, 128, 2048, seed=18, ignore_frac=0.25)
     X, W, y = make_inputs(wl)
-    r1 = GpuRun(X, W, y)
+    r1 = CudaRun(X, W, y)
     assert r1.forward() == 0 and r1.backward() == 0
     a = r1.host()
     X2 = X.clone()
     ign = (y == IGNORE_INDEX)
     X2[ign] = (X2[ign].float() * -3.0 + 1.0).bfloat16()
-    r2 = GpuRun(X2, W, y)
+    r2 = CudaRun(X2, W, y)
     assert r2.forward() == 0 and r2.backward() == 0
     b = r2.host()
     assert np.array_equal(a["loss"], b["loss"])

@@ -8,14 +8,14 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, GpuRun, rel_fro
+from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, TOL_LOSS_REL, TOL_LSE_ABS, CudaRun, rel_fro
 from workloads import WORKLOADS, make_inputs, sample_indices
 
 pytestmark = pytest.mark.gpu
 
 
 def _gpu(wl, X, W, y):
-    run = GpuRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
     assert run.forward() == 0
     assert run.backward() == 0
     return run.host()

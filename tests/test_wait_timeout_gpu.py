@@ -10,7 +10,7 @@ import torch
 
 import linear_cross_entropy_tcgen05_gb300 as flce
 import oracle
-from tests.flce_cases import TOL_LOSS_REL, GpuRun
+from tests.flce_cases import TOL_LOSS_REL, CudaRun
 from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -29,7 +29,7 @@ def test_a_wait_that_runs_out_reports_a_timeout_and_the_context_survives(gpu_lib
     # the next call on the same context works and is correct
     wl = WORKLOADS["tiny"]
     X, W, y = make_inputs(wl)
-    run = GpuRun(X, W, y)
+    run = CudaRun(X, W, y)
     assert run.forward() == 0
     assert run.backward() == 0
     loss, _, _, _ = oracle.forward_backward(X, W, y)

@@ -2,7 +2,8 @@
 
 The translation units compile in parallel with nvcc and link into one shared
 library with a static CUDA runtime, so loading it needs no driver library until the
-first CUDA call. Run ``python -m linear_cross_entropy_tcgen05_gb300.build``.
+first CUDA call. Run ``python -m linear_cross_entropy_tcgen05_gb300.build``, optionally
+with ``-DNAME=VALUE`` compile-time tunables.
 """
 from __future__ import annotations
 
@@ -60,4 +61,7 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    # python -m linear_cross_entropy_tcgen05_gb300.build [-v] [-DNAME=VALUE ...]
+    # -D sets a compile-time tunable of the kernels (e.g. -DFLCE_FWD_GN=1).
+    defines = [a for a in sys.argv[1:] if a.startswith("-D")]
+    print(build(verbose="-v" in sys.argv, extra=defines))

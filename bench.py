@@ -148,13 +148,16 @@ def barrier(world: int):
         dist.barrier()
 
 
-def kernel_launches_per_step(N, D, V, reduction):
+def kernel_launches_per_step(N, D, V, reduction, vc=None):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
-    backward denominator + row coefficients + 3 GEMMs per vocabulary band + the dX cast."""
-    unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
-    vc = max(unit, min(16384, ((1 << 30) // (2 * N)) // unit * unit))
-    half = (((V + 1) // 2) + unit - 1) // unit * unit
-    vc = min(vc, half)
+    backward denominator + row coefficients + 3 GEMMs per vocabulary band + the dX cast.
+    vc is the band width (flce_backward_band_width on the device); without it, the
+    workspace's band capacity."""
+    if vc is None:
+        unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
+        vc = max(unit, min(16384, ((1 << 30) // (2 * N)) // unit * unit))
+        half = (((V + 1) // 2) + unit - 1) // unit * unit
+        vc = min(vc, half)
     bands = -(-V // vc)
     fwd = 1 + 1 + (0 if reduction == "none" else 1)
     bwd = 2 + 3 * bands + 1
@@ -318,7 +321,8 @@ def run_ours(args, wl, world, rank, local):
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
     e2e_value, e2e_ms, h2d, d2h = run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd)
     return finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc,
-                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed)
+                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed,
+                  flce.flce_backward_band_width(N, D, V) or None)
 
 
 def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
@@ -395,7 +399,7 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
 
 
 def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
-           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed):
+           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -404,7 +408,7 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
     bwd_tf = 6.0 * N * D * V / (statistics.mean(bwd_ms) / 1000.0) / 1e12
     burst = float(peaks["bf16_tflops"])
     sustained = float(peaks.get("bf16_tflops_sustained", burst))
-    launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction)
+    launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width)
 
     if rank != 0:
         return

@@ -254,6 +254,13 @@ const char* flce_last_error_detail(void);
  * For profiling and launch accounting; the pages have no counterpart. */
 unsigned long long flce_kernel_launches(void);
 
+/* Width (vocabulary columns) of the gradient bands flce_backward uses for this shape on
+ * the current device: a multiple of 512 at most the workspace's band capacity, chosen so
+ * that the dW GEMM's launches fill the device's resident clusters evenly. opt may be
+ * NULL (only weight_layout and row_band matter). Returns 0 for invalid sizes or without
+ * a supported device. Diagnostics and launch accounting; the pages have no counterpart. */
+int64_t flce_backward_band_width(int64_t N, int64_t D, int64_t V, const flce_options* opt);
+
 /* Self-test of failure detection: launches one small kernel whose pipeline wait (the
  * bounded mbarrier wait every GEMM uses) waits for an arrival that never comes, gives up
  * after the wait limit (2 s) and records FLCE_DEVERR_TIMEOUT in the workspace header

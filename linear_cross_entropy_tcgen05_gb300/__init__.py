@@ -43,7 +43,7 @@ EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flc
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
                     "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards",
                     "flce_last_error_detail", "flce_shard_stats_ex", "flce_kernel_launches",
-                    "flce_selftest_wait_timeout")
+                    "flce_selftest_wait_timeout", "flce_backward_band_width")
 
 
 class FlceOptions(ctypes.Structure):
@@ -131,6 +131,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_kernel_launches.restype = ctypes.c_ulonglong
     lib.flce_selftest_wait_timeout.argtypes = [vp, sz, vp]
     lib.flce_selftest_wait_timeout.restype = ctypes.c_int
+    lib.flce_backward_band_width.argtypes = [i64, i64, i64, vp]
+    lib.flce_backward_band_width.restype = i64
     op = ctypes.POINTER(FlceOptions)
     lib.flce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp, sz, vp]
     lib.flce_forward_ex.restype = ctypes.c_int
@@ -163,6 +165,11 @@ def flce_selftest_wait_timeout(workspace, stream=None) -> int:
     """Launch the bounded-wait self-test (returns the launch status; read the outcome
     with flce_check_device_error, which should give FLCE_ERR_TIMEOUT after ~2 s)."""
     return int(load_library().flce_selftest_wait_timeout(_ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def flce_backward_band_width(N: int, D: int, V: int, options: FlceOptions | None = None) -> int:
+    """Vocabulary columns per gradient band that flce_backward uses on this device (0 if none)."""
+    return int(load_library().flce_backward_band_width(N, D, V, _opt_ref(options)))
 
 
 def flce_kernel_launches() -> int:

@@ -35,6 +35,9 @@ namespace {
 #ifndef FLCE_BAND_W_L2_BYTES
 #define FLCE_BAND_W_L2_BYTES int64_t(0)  // if > 0: also cap the band so its W slice (2*D*Vc) fits this
 #endif
+#ifndef FLCE_BAND_PICK
+#define FLCE_BAND_PICK 1  // 1: pick the band width for even dW waves; 0: the workspace's capacity
+#endif
 #ifndef FLCE_FWD_GN
 #define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
 #endif
@@ -101,6 +104,40 @@ int64_t band_width(int64_t N, int64_t D, int64_t V) {
   const int64_t half = cdiv(cdiv(V, 2), unit) * unit;
   if (vc > half) vc = half;
   return vc;
+}
+
+// Launch units (clusters' worth of tiles) of the dW GEMM over a band of vc columns.
+int64_t dw_units(int64_t vc, int64_t D, bool w_vd) {
+  const int64_t mc = gemm_pairs_per_cluster();
+  if (w_vd) return cdiv(cdiv(vc, gemm_tile_rows()), mc) * cdiv(D, kBN);
+  return cdiv(cdiv(D, gemm_tile_rows()), mc) * cdiv(vc, kBN);
+}
+
+// The band width the backward uses for `rows` rows on a device with `clusters` resident
+// clusters: among the multiples of 512 in [cap/2, cap], the one with the least estimated
+// dW time. The dW GEMM has few, long tiles (K = rows), so it runs in whole waves of
+// `clusters` units: a band of 32 vocabulary tiles on 36 clusters (8 units each) takes 8
+// waves for 7.1 waves of work. The estimate counts waves over all bands plus, per band,
+// ~20 us of launch ramp and tail, i.e. 4000/rows of a wave (a dW unit moves through K at
+// ~5 ns per row). The gradient and dX GEMMs have thousands of short tiles and do not
+// care. Ties keep the wider band. The workspace is sized for `cap`.
+int64_t pick_band_width(int64_t cap, int64_t rows, int64_t D, int64_t V, bool w_vd, int clusters) {
+  const int64_t unit = int64_t(gemm_tile_rows()) * gemm_pairs_per_cluster();
+  if (!FLCE_BAND_PICK || clusters <= 0 || rows <= 0) return cap;
+  const double band_cost = 4000.0 / double(rows);
+  int64_t best = cap;
+  double best_cost = 0.0;
+  for (int64_t vc = cap; vc >= unit && 2 * vc >= cap; vc -= unit) {
+    int64_t waves = 0, bands = 0;
+    for (int64_t v0 = 0; v0 < V; v0 += vc, ++bands)
+      waves += cdiv(dw_units(V - v0 < vc ? V - v0 : vc, D, w_vd), clusters);
+    const double cost = double(waves) + band_cost * double(bands);
+    if (vc == cap || cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = vc;
+    }
+  }
+  return best;
 }
 
 BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
@@ -458,7 +495,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   void* band = ws + L.band;
   float* dx_acc = reinterpret_cast<float*>(ws + L.dx_acc);
   const bool f32_out = opt && opt->dX_f32;
-  const int64_t Vc = L.Vc;
+  const int64_t Vc = pick_band_width(L.Vc, Nb, pb.D, pb.V, pb.w_vd, walk_max_clusters());
   const bool shard = opt && opt->v_total != 0 && opt->v_total != pb.V;
   const int64_t V_total = shard ? opt->v_total : pb.V;
   const int64_t v_offset = shard ? opt->v_offset : 0;
@@ -782,6 +819,15 @@ flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* ta
   f.err = reinterpret_cast<int*>(ws + kHdrErr);
   FLCE_CUDA_CHECK(launch_finalize(f, L.blocks, s));
   return FLCE_OK;
+}
+
+int64_t flce_backward_band_width(int64_t N, int64_t D, int64_t V, const flce_options* opt) {
+  if (!sizes_ok(N, D, V) || !sizes_in_range(N, D, V)) return 0;
+  int sms = 0;
+  if (current_device(&sms) != FLCE_OK) return 0;
+  const int64_t rows = backward_rows(opt, N);
+  const BwdLayout L = bwd_layout(rows, D, V);
+  return pick_band_width(L.Vc, rows, D, V, opt_w_vd(opt), walk_max_clusters());
 }
 
 flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream_) {

@@ -1043,6 +1043,9 @@ int gemm_b_rows_per_cta() { return Geo<kCG>::kBRows; }
 // Every forward instantiation has the same launch shape (shared memory and threads).
 int forward_max_units() { return max_clusters(fwd_kernel<true, false, false>(), kFwdSmem, 0); }
 
+// Every walk instantiation has the same launch shape too.
+int walk_max_clusters() { return max_clusters(dw_kernel<false>(), kWalkSmem, 2); }
+
 namespace {
 template <bool F16>
 auto pick_fwd(bool ext, bool w_vd) {

@@ -200,6 +200,8 @@ int gemm_pairs_per_cluster();
 int gemm_b_rows_per_cta();
 // CTA pairs of the forward GEMM that can be resident at once on the current device.
 int forward_max_units();
+// Clusters of the backward GEMMs that can be resident at once on the current device.
+int walk_max_clusters();
 
 // ext: the extended epilogue (bias, softcap, class weights, argmax); else the plain one.
 // w_vd: W is stored [V, D] (B is K-major); else [D, V] (B is MN-major).

@@ -138,6 +138,7 @@ def test_refuses_without_a_supported_device(lib):
     assert lib.flce_selftest_wait_timeout(0x60000, 4096, None) == 3
     assert lib.flce_selftest_wait_timeout(None, 4096, None) == 1
     assert lib.flce_selftest_wait_timeout(0x60000, 16, None) == 4
+    assert flce.flce_backward_band_width(65536, 4096, 128256) == 0   # depends on the device
 
 
 def test_options_struct_matches_the_header():

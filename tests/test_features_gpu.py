@@ -266,5 +266,7 @@ def test_launch_counter_matches_the_band_schedule(gpu_lib):
     flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws)
     counted = flce.flce_kernel_launches() - before
     assert flce.flce_check_device_error(ws) == 0
-    expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean")
-    assert bands == 2 and counted == expected
+    vc = flce.flce_backward_band_width(N, D, V)
+    assert vc > 0 and vc % 512 == 0
+    expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean", vc)
+    assert bands == -(-V // vc) and counted == expected

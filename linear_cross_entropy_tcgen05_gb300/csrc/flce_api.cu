@@ -38,6 +38,9 @@ namespace {
 #ifndef FLCE_BAND_PICK
 #define FLCE_BAND_PICK 1  // 1: pick the band width for even dW waves; 0: the workspace's capacity
 #endif
+#ifndef FLCE_DW_TRANSPOSE_ODD
+#define FLCE_DW_TRANSPOSE_ODD 1  // 1: G^T X with a transposed store when D's row tiles are odd
+#endif
 #ifndef FLCE_FWD_GN
 #define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
 #endif
@@ -106,10 +109,18 @@ int64_t band_width(int64_t N, int64_t D, int64_t V) {
   return vc;
 }
 
+// The dW GEMM computes G^T X (tile rows = vocabulary, the pairs of a cluster on
+// neighbouring vocabulary tiles) for a [V, D] dW, and also for a [D, V] dW when D's row
+// tiles do not split evenly among a cluster's pairs (the extra pair would compute zeros);
+// its epilogue then stores the tiles transposed. Otherwise it computes X^T G.
+bool dw_vocab_rows(int64_t D, bool w_vd) {
+  return w_vd || (FLCE_DW_TRANSPOSE_ODD && cdiv(D, gemm_tile_rows()) % gemm_pairs_per_cluster() != 0);
+}
+
 // Launch units (clusters' worth of tiles) of the dW GEMM over a band of vc columns.
-int64_t dw_units(int64_t vc, int64_t D, bool w_vd) {
+int64_t dw_units(int64_t vc, int64_t D, bool vocab_rows) {
   const int64_t mc = gemm_pairs_per_cluster();
-  if (w_vd) return cdiv(cdiv(vc, gemm_tile_rows()), mc) * cdiv(D, kBN);
+  if (vocab_rows) return cdiv(cdiv(vc, gemm_tile_rows()), mc) * cdiv(D, kBN);
   return cdiv(cdiv(D, gemm_tile_rows()), mc) * cdiv(vc, kBN);
 }
 
@@ -130,7 +141,7 @@ int64_t pick_band_width(int64_t cap, int64_t rows, int64_t D, int64_t V, bool w_
   for (int64_t vc = cap; vc >= unit && 2 * vc >= cap; vc -= unit) {
     int64_t waves = 0, bands = 0;
     for (int64_t v0 = 0; v0 < V; v0 += vc, ++bands)
-      waves += cdiv(dw_units(V - v0 < vc ? V - v0 : vc, D, w_vd), clusters);
+      waves += cdiv(dw_units(V - v0 < vc ? V - v0 : vc, D, dw_vocab_rows(D, w_vd)), clusters);
     const double cost = double(waves) + band_cost * double(bands);
     if (vc == cap || cost < best_cost - 1e-9) {
       best_cost = cost;
@@ -239,13 +250,15 @@ flce_status current_device(int* sms) {
 
 // 2-D row-major tensor [outer][inner] with row pitch `pitch_elems`, 128-byte swizzled boxes.
 bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
+               bool swizzle = true) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {pitch_elems * uint64_t(elem_bytes)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
   return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS ||
          (note_error("cuTensorMapEncodeTiled", "the tensor map was refused"), false);
 }
@@ -509,12 +522,14 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const uint64_t w_inner = pb.w_vd ? uint64_t(pb.D) : uint64_t(pb.V);
   const uint64_t w_outer = pb.w_vd ? uint64_t(pb.V) : uint64_t(pb.D);
   const uint32_t kmaj_rows = uint32_t(gemm_b_rows_per_cta());
-  CUtensorMap tmWg, tmWx, tmDW;
+  CUtensorMap tmWg, tmWx, tmDW, tmDWt;
   if (!encode_2d(&tmWg, pb.dt16(), 2, pb.W, w_inner, w_outer, w_inner, 64,
                  pb.w_vd ? kmaj_rows : 64) ||
       !encode_2d(&tmWx, pb.dt16(), 2, pb.W, w_inner, w_outer, w_inner, 64,
                  pb.w_vd ? 64 : kmaj_rows) ||
-      !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, w_inner, w_outer, w_inner, 32, kBM))
+      !encode_2d(&tmDW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, w_inner, w_outer, w_inner, 32, kBM) ||
+      // [D, V] dW written from G^T X tiles: 32 rows of D x 128 vocabulary columns, unswizzled
+      !encode_2d(&tmDWt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, w_inner, w_outer, w_inner, kBM, 32, false))
     return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
@@ -604,24 +619,30 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         FLCE_CUDA_CHECK(launch_colsum(cp, stream));
       }
 
-      // dW = X^T G (K = rows of the band); later row bands add into dW. For a [V, D] dW the
-      // GEMM computes G^T X instead: the operands swap, rows are vocabulary tiles.
+      // dW = X^T G (K = rows of the band); later row bands add into dW. With vocabulary
+      // rows the GEMM computes G^T X instead (the operands swap): stored as it is into a
+      // [V, D] dW, transposed into a [D, V] one.
       WalkParams ww{};
       ww.num_kb = int(cdiv(nb, kBK));
       StoreEpiParams sw{n0 > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
-      if (!pb.w_vd) {
+      if (!dw_vocab_rows(pb.D, pb.w_vd)) {
         ww.total_tiles = int(vt * d_tiles_m);
         ww.tiles_minor = int(d_tiles_m);
         ww.col_major = 1;
         sw.x_off = int(v0);
-        FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, pb.f16, stream));
+        FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, false, pb.f16, stream));
       } else {
         const int64_t v_groups = cdiv(cdiv(vc, gemm_tile_rows()), mc);
         ww.total_tiles = int(v_groups * d_tiles_n);
         ww.tiles_minor = int(d_tiles_n);
         ww.col_major = 0;
-        sw.y_off = int(v0);
-        FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDW, ww, sw, pb.f16, stream));
+        if (pb.w_vd) {
+          sw.y_off = int(v0);
+          FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDW, ww, sw, false, pb.f16, stream));
+        } else {
+          sw.x_off = int(v0);  // the tile's vocabulary rows land on dW columns v0 + ...
+          FLCE_CUDA_CHECK(launch_dw_gemm(tmGmn, tmXmn, tmDWt, ww, sw, true, pb.f16, stream));
+        }
       }
 
       WalkParams wx{};

@@ -919,12 +919,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 32; ++q) r0[q] = __float_as_uint(__uint_as_float(r0[q]) * out_scale);
           }
-          uint4 chunks[8];
+          if constexpr (EPI == 2) {
+            // transposed store: the tile's rows become the destination's columns. The box is
+            // 32 destination rows x 128 columns, unswizzled; thread r writes column r, so a
+            // warp writes 128 contiguous bytes of each row.
+            epi_store_box(
+                s, epi_tid, box_idx++,
+                [&](uint8_t* box) {
+                  float* b = reinterpret_cast<float*>(box);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
-          epi_store_box(
-              s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
-              sp.x_off + t.b_row + c, sp.y_off + t.a_row, sp.reduce_add != 0, store_hint, pol_store);
+                  for (int q = 0; q < 32; ++q) b[q * kBM + r] = __uint_as_float(r0[q]);
+                },
+                &tmC, sp.x_off + t.a_row, sp.y_off + t.b_row + c, sp.reduce_add != 0, store_hint, pol_store);
+          } else {
+            uint4 chunks[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              chunks[q] = make_uint4(r0[4 * q], r0[4 * q + 1], r0[4 * q + 2], r0[4 * q + 3]);
+            epi_store_box(
+                s, epi_tid, box_idx++, [&](uint8_t* box) { staging_write_row(box, r, chunks); }, &tmC,
+                sp.x_off + t.b_row + c, sp.y_off + t.a_row, sp.reduce_add != 0, store_hint, pol_store);
+          }
         }
       }
       acc ^= 1;
@@ -1008,8 +1023,9 @@ template <bool B_MN, bool F16, bool EXT>
 auto fwd_kernel() { return flce_forward_gemm_kernel<kCG, kMC, kFwdStages, B_MN, F16, EXT>; }
 template <bool B_MN, bool F16, bool EXT>
 auto grad_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, F16, WALK_GRAD, 0, EXT>; }
-template <bool F16>
-auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, F16, WALK_DW, 1, false>; }
+// EPI 1 stores tiles as they are, EPI 2 transposed (a [D, V] dW computed as G^T X).
+template <bool F16, int EPI = 1>
+auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, true, F16, WALK_DW, EPI, false>; }
 template <bool B_MN, bool F16>
 auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, F16, WALK_DX, 1, false>; }
 
@@ -1085,9 +1101,14 @@ cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, con
 }
 
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, bool f16, cudaStream_t stream) {
+                           const WalkParams& w, const StoreEpiParams& e, bool transposed_store, bool f16,
+                           cudaStream_t stream) {
   GradEpiParams unused{};
   unused.err = e.err;
+  if (transposed_store) {
+    if (f16) return launch_walk(dw_kernel<true, 2>(), tmA, tmB, tmC, w, unused, e, 2, stream);
+    return launch_walk(dw_kernel<false, 2>(), tmA, tmB, tmC, w, unused, e, 2, stream);
+  }
   if (f16) return launch_walk(dw_kernel<true>(), tmA, tmB, tmC, w, unused, e, 2, stream);
   return launch_walk(dw_kernel<false>(), tmA, tmB, tmC, w, unused, e, 2, stream);
 }

@@ -222,12 +222,14 @@ cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream);
 // The walk GEMMs size their own grids: min(tile groups, resident clusters) clusters.
 // w_vd as in launch_forward_gemm: it sets the major-ness of W, the B operand of the
 // gradient and dX GEMMs. The dW GEMM takes both operands MN-major in either layout (the
-// caller swaps them for a [V, D] dW).
+// caller swaps them to compute G^T X, rows = vocabulary tiles); transposed_store writes
+// such G^T X tiles into a [D, V] dW through an unswizzled 128 x 32 box.
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                              const WalkParams& w, const GradEpiParams& e, bool ext, bool w_vd, bool f16,
                              cudaStream_t stream);
 cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                           const WalkParams& w, const StoreEpiParams& e, bool f16, cudaStream_t stream);
+                           const WalkParams& w, const StoreEpiParams& e, bool transposed_store, bool f16,
+                           cudaStream_t stream);
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, bool w_vd, bool f16, cudaStream_t stream);
 // fp32 -> bf16 (or f16) of n elements, n a multiple of 4.

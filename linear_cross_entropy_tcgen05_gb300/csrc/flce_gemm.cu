@@ -26,12 +26,14 @@
 //               Implementation"; Liger-Kernel PR #1291 "Summary": a store-free forward
 //               that keeps only the per-row LSE and target logit.)
 //   gradient  : recomputed logits -> G = g[p(1+2s lse) - (1-eps) onehot - eps/V] in
-//               registers, rounded to bf16 and stored by TMA into the gradient band.
-//               ("Cross-Entropy" and "Fused Linear Cross-Entropy" of the same post;
-//               the smoothing rule of TransformerEngine PR #995's backward kernel.)
+//               registers, rounded to bf16 (or f16, scaled) and stored by TMA into the
+//               gradient band. ("Cross-Entropy" and "Fused Linear Cross-Entropy" of the
+//               same post; the smoothing rule of TransformerEngine PR #995's backward
+//               kernel.)
 //   dW / dX   : fp32 accumulator -> shared memory -> TMA store (dW, each block written
-//               once) or TMA element-wise add (dX accumulation across vocabulary bands,
-//               each element touched by one tile per launch, so no races).
+//               once, as it is or transposed) or TMA element-wise add (dX accumulation
+//               across vocabulary bands, each element touched by one tile per launch, so
+//               no races).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>

@@ -155,7 +155,7 @@ def kernel_launches_per_step(N, D, V, reduction, vc=None):
     workspace's band capacity."""
     if vc is None:
         unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
-        vc = max(unit, min(16384, ((1 << 30) // (2 * N)) // unit * unit))
+        vc = max(unit, min(16384, ((3 << 28) // (2 * N)) // unit * unit))
         half = (((V + 1) // 2) + unit - 1) // unit * unit
         vc = min(vc, half)
     bands = -(-V // vc)

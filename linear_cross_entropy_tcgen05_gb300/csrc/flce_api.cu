@@ -30,7 +30,9 @@ namespace {
 
 // Compile-time tunables (defaults are the measured choices).
 #ifndef FLCE_BAND_BYTES
-#define FLCE_BAND_BYTES (int64_t(1) << 30)  // byte budget of the bf16 gradient band
+// Byte budget of the 16-bit gradient band: 768 MiB keeps the backward's workspace (band +
+// fp32 dX accumulator) under an eighth of the bf16 logits at N = 65536, V = 128256.
+#define FLCE_BAND_BYTES (int64_t(3) << 28)
 #endif
 #ifndef FLCE_BAND_W_L2_BYTES
 #define FLCE_BAND_W_L2_BYTES int64_t(0)  // if > 0: also cap the band so its W slice (2*D*Vc) fits this

@@ -69,7 +69,7 @@ def test_workspace_sizes(lib):
     N, D, V = 65536, 4096, 128256
     wb = flce.flce_workspace_size(N, D, V, True)
     logits_bf16 = flce.logits_bytes(N, V, 2)
-    assert wb < logits_bf16 / 4, "the backward workspace must be far below an N x V bf16 buffer"
+    assert wb < logits_bf16 / 8, "the backward workspace must stay under an eighth of an N x V bf16 buffer"
     assert wb >= N * D * 4  # holds the fp32 dX accumulator
     # every band is narrower than the vocabulary once V exceeds one 256-column tile
     for (n, d, v) in [(256, 128, 1024), (4096, 2048, 32000), (8192, 4096, 128256), (16384, 2304, 256000)]:

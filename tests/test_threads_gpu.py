@@ -51,3 +51,40 @@ def test_first_call_on_a_fresh_thread(gpu_lib):
     torch.cuda.synchronize()
     for k in ("loss", "lse", "dX", "dW"):
         assert torch.equal(main[k], other[k]), k
+
+
+def test_two_threads_on_two_streams(gpu_lib):
+    """Two threads, each with its own stream and workspace, run forward + backward at the
+    same time; each result equals the one-thread result bit for bit."""
+    wl = custom("thread2", 768, 256, 4104, seed=52, ignore_frac=0.1, label_smoothing=0.1)
+    X, W, y = make_inputs(wl)
+    X2, _, y2 = make_inputs(wl, seed=53)
+    Wd = W.to(DEV)
+    g = torch.ones(1, device=DEV)
+    inputs = [(X.to(DEV), y.to(DEV)), (X2.to(DEV), y2.to(DEV))]
+    want = []
+    for Xd, yd in inputs:
+        b = _buffers(wl.N, wl.D, wl.V)
+        assert _step(Xd, Wd, yd, g, b, torch.cuda.current_stream(DEV).cuda_stream) == (0, 0)
+        torch.cuda.synchronize()
+        want.append(b)
+    streams = [torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)]
+    got = [_buffers(wl.N, wl.D, wl.V) for _ in inputs]
+    torch.cuda.synchronize()
+    status = [None, None]
+
+    def work(i):
+        for _ in range(3):
+            status[i] = _step(inputs[i][0], Wd, inputs[i][1], g, got[i], streams[i].cuda_stream)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert status == [(0, 0), (0, 0)]
+    for i in range(2):
+        assert flce.flce_check_device_error(got[i]["ws"]) == 0
+        for k in ("loss", "lse", "dX", "dW"):
+            assert torch.equal(got[i][k], want[i][k]), (i, k)

@@ -173,6 +173,10 @@ typedef struct flce_options {
                                 accumulates across bands (fp32 adds in a fixed order). 0: all rows. */
   int32_t weight_layout;     /* flce_weight_layout of W and dW (FLCE_WEIGHT_DV if 0) */
   int32_t input_dtype;       /* flce_input_dtype of X, W and dX (FLCE_INPUT_BF16 if 0) */
+  int32_t accumulate_grads;  /* backward: 1 adds this call's dW (and dbias) into the caller's
+                                buffers instead of overwriting them, for gradient accumulation
+                                over micro-batches ([P1] "Path to Production"); the adds are
+                                fp32 element-wise, in a fixed order. dX is always overwritten. */
 } flce_options;
 
 /* flce_forward with options (NULL behaves exactly like flce_forward). Vocabulary

@@ -52,7 +52,8 @@ class FlceOptions(ctypes.Structure):
     _fields_ = [("softcap", ctypes.c_float), ("bias", ctypes.c_void_p), ("class_weight", ctypes.c_void_p),
                 ("predicted", ctypes.c_void_p), ("accuracy", ctypes.c_void_p), ("dbias", ctypes.c_void_p),
                 ("dX_f32", ctypes.c_void_p), ("v_offset", ctypes.c_int64), ("v_total", ctypes.c_int64),
-                ("row_band", ctypes.c_int64), ("weight_layout", ctypes.c_int32), ("input_dtype", ctypes.c_int32)]
+                ("row_band", ctypes.c_int64), ("weight_layout", ctypes.c_int32), ("input_dtype", ctypes.c_int32),
+                ("accumulate_grads", ctypes.c_int32)]
 
 
 def _layout(weight_layout) -> int:
@@ -67,11 +68,11 @@ def _dtype_code(input_dtype) -> int:
 
 def make_options(softcap: float = 0.0, bias=None, class_weight=None, predicted=None, accuracy=None, dbias=None,
                  dX_f32=None, v_offset: int = 0, v_total: int = 0, row_band: int = 0, weight_layout="dv",
-                 input_dtype="bf16"):
+                 input_dtype="bf16", accumulate_grads: bool = False):
     """An ``flce_options`` value (device tensors become pointers)."""
     return FlceOptions(float(softcap), _ptr(bias), _ptr(class_weight), _ptr(predicted), _ptr(accuracy),
                        _ptr(dbias), _ptr(dX_f32), int(v_offset), int(v_total), int(row_band),
-                       _layout(weight_layout), _dtype_code(input_dtype))
+                       _layout(weight_layout), _dtype_code(input_dtype), 1 if accumulate_grads else 0)
 
 
 def _check_dtype(X, options) -> None:

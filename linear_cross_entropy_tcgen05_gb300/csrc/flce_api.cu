@@ -395,6 +395,7 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
   if (o->row_band < 0) return FLCE_ERR_INVALID_ARG;
   if (o->weight_layout != FLCE_WEIGHT_DV && o->weight_layout != FLCE_WEIGHT_VD) return FLCE_ERR_INVALID_ARG;
   if (o->input_dtype != FLCE_INPUT_BF16 && o->input_dtype != FLCE_INPUT_F16) return FLCE_ERR_INVALID_ARG;
+  if (o->accumulate_grads != 0 && o->accumulate_grads != 1) return FLCE_ERR_INVALID_ARG;
   const bool shard = o->v_total != 0 && o->v_total != pb.V;
   if (shard) {
     if (!backward) return FLCE_ERR_INVALID_ARG;  // forward shards go through flce_shard_stats
@@ -517,6 +518,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const float* cw = opt ? opt->class_weight : nullptr;
   const bool ext = opt_ext_grad(opt);
   const float* out_scale = pb.f16 ? gval : nullptr;  // dW, dX = g / kF16GradScale * (f16 band GEMM)
+  const bool add_grads = opt && opt->accumulate_grads;  // dW (and dbias) += this call's gradient
 
   // Maps that do not depend on the row band. tmWg: B of the gradient GEMM (N = vocabulary,
   // K = D); tmWx: B of the dX GEMM (N = D, K = vocabulary). Each is MN-major in one W layout
@@ -614,7 +616,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         cp.row_chunks = kColsumChunks;
         cp.partial = reinterpret_cast<float*>(ws + L.colsum);
         cp.out = opt->dbias + v0;
-        cp.accumulate = n0 > 0 ? 1 : 0;
+        cp.accumulate = (n0 > 0 || add_grads) ? 1 : 0;
         cp.f16 = pb.f16 ? 1 : 0;
         cp.scale = pb.f16 ? gval : nullptr;
         cp.scale_mul = 1.f / kF16GradScale;
@@ -626,7 +628,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       // [V, D] dW, transposed into a [D, V] one.
       WalkParams ww{};
       ww.num_kb = int(cdiv(nb, kBK));
-      StoreEpiParams sw{n0 > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
+      StoreEpiParams sw{(n0 > 0 || add_grads) ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
       if (!dw_vocab_rows(pb.D, pb.w_vd)) {
         ww.total_tiles = int(vt * d_tiles_m);
         ww.tiles_minor = int(d_tiles_m);
@@ -779,7 +781,7 @@ flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* tar
   if (opt) {
     // only the storage options apply to shard statistics
     if (opt->softcap != 0.f || opt->bias || opt->class_weight || opt->predicted || opt->accuracy || opt->dbias ||
-        opt->dX_f32 || opt->v_offset != 0 || opt->v_total != 0 || opt->row_band != 0)
+        opt->dX_f32 || opt->v_offset != 0 || opt->v_total != 0 || opt->row_band != 0 || opt->accumulate_grads)
       return FLCE_ERR_INVALID_ARG;
     if (opt->weight_layout != FLCE_WEIGHT_DV && opt->weight_layout != FLCE_WEIGHT_VD) return FLCE_ERR_INVALID_ARG;
     if (opt->input_dtype != FLCE_INPUT_BF16 && opt->input_dtype != FLCE_INPUT_F16) return FLCE_ERR_INVALID_ARG;

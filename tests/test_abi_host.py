@@ -220,6 +220,7 @@ def test_option_checks(lib):
     assert _fwd_ex(lib, _opts(weight_layout=2)) == 1        # not a flce_weight_layout
     assert _bwd_ex(lib, _opts(weight_layout=-1)) == 1
     assert _fwd_ex(lib, _opts(input_dtype=2)) == 1          # not a flce_input_dtype
+    assert _bwd_ex(lib, flce.FlceOptions(accumulate_grads=2)) == 1  # not 0 or 1
     for bad in (_opts(softcap=2.0), _opts(row_band=64), _opts(weight_layout=3)):  # storage options only
         assert lib.flce_shard_stats_ex(0x10000, 0x20000, 0x30000, 256, 128, 1024, 0, -100, ctypes.byref(bad),
                                        0x40000, 0x60000, 1 << 20, None) == 1

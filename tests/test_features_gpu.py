@@ -270,3 +270,40 @@ def test_launch_counter_matches_the_band_schedule(gpu_lib):
     assert vc > 0 and vc % 512 == 0
     expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean", vc)
     assert bands == -(-V // vc) and counted == expected
+
+
+def test_gradient_accumulation_over_micro_batches(gpu_lib):
+    """accumulate_grads: dW and dbias of two micro-batches (sum reduction) added into the
+    same buffers equal one call over the whole batch (to fp32 rounding) and the oracle."""
+    wl = custom("accum", 1000, 136, 4104, seed=38, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-3,
+                reduction="sum")
+    X, W, y, bias, _ = _inputs(wl)
+    N, D, V = wl.N, wl.D, wl.V
+    Wd, bd = W.to(DEV), bias.to(DEV)
+    common = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "sum")
+    g = torch.ones(1, device=DEV)
+    dW = torch.full((D, V), float("nan"), device=DEV)
+    db = torch.full((V,), float("nan"), device=DEV)
+    for i, (a, b) in enumerate([(0, 600), (600, N)]):
+        Xm, ym = X[a:b].contiguous().to(DEV), y[a:b].contiguous().to(DEV)
+        n = b - a
+        ws = _ws(n, D, V, 2)
+        loss, lse = torch.empty(1, device=DEV), torch.empty(n, device=DEV)
+        dX = torch.empty(n, D, dtype=torch.bfloat16, device=DEV)
+        opts = flce.make_options(bias=bd, dbias=db, accumulate_grads=i > 0)
+        flce.flce_forward_backward(Xm, Wd, ym, g, loss, lse, dX, dW, ws, *common, options=opts)
+        assert flce.flce_check_device_error(ws) == 0
+    torch.cuda.synchronize()
+    _, _, _, ref_dW, ref_db = oracle.forward_backward_ext(X, W, y, *common, bias=bias)
+    assert rel_fro(dW.cpu().numpy(), ref_dW) <= TOL_DW_REL
+    assert rel_fro(db.cpu().numpy(), ref_db) <= TOL_DW_REL
+    # one call over the whole batch gives the same dW up to the order of fp32 additions
+    ws = _ws(N, D, V, 2)
+    dW1 = torch.empty(D, V, device=DEV)
+    db1 = torch.empty(V, device=DEV)
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    flce.flce_forward_backward(X.to(DEV), Wd, y.to(DEV), g, loss, lse, torch.empty(N, D, dtype=torch.bfloat16,
+                               device=DEV), dW1, ws, *common, options=flce.make_options(bias=bd, dbias=db1))
+    torch.cuda.synchronize()
+    assert rel_fro(dW.cpu().numpy(), dW1.cpu().numpy()) <= 1e-5
+    assert rel_fro(db.cpu().numpy(), db1.cpu().numpy()) <= 1e-5

@@ -242,7 +242,9 @@ flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream)
 /* A static, human-readable name for a status. */
 const char* flce_status_string(flce_status status);
 
-/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH: 200 (0.2.0). 0.2 grew flce_options
+ * (weight_layout, input_dtype, accumulate_grads at its end): code built against 0.1's
+ * header must be rebuilt. */
 int flce_version(void);
 
 /* Which call failed the last time an entry point returned FLCE_ERR_CUDA on the calling

@@ -312,7 +312,7 @@ void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc,
 
 extern "C" {
 
-int flce_version(void) { return 100; }
+int flce_version(void) { return 200; }
 
 const char* flce_last_error_detail(void) { return g_detail; }
 

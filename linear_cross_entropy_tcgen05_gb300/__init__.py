@@ -26,6 +26,7 @@ __all__ = [
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
     "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail", "flce_kernel_launches",
+    "flce_selftest_wait_timeout", "flce_backward_band_width",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

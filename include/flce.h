@@ -83,7 +83,9 @@ typedef enum {
   FLCE_ERR_CUDA = 6,                 /* a CUDA runtime or driver call failed */
   FLCE_ERR_BAD_TARGET = 7,           /* device: a target outside [0,V) that is not ignore_index */
   FLCE_ERR_TIMEOUT = 8,              /* device: a pipeline wait exceeded its limit; results invalid */
-  FLCE_ERR_TOO_LARGE = 9             /* a size exceeds the library's index range */
+  FLCE_ERR_TOO_LARGE = 9,            /* a size exceeds the library's index range */
+  FLCE_ERR_F16_RANGE = 10            /* device, f16 inputs: a row's scaled gradient coefficient
+                                        exceeds the f16 range (class weights too large) */
 } flce_status;
 
 typedef enum {
@@ -153,7 +155,8 @@ typedef enum { FLCE_WEIGHT_DV = 0, FLCE_WEIGHT_VD = 1 } flce_weight_layout;
  * both at the same rate. With f16 the gradient band holds G/g scaled by 2^10 (so that
  * probabilities near 1/V stay normal f16 numbers) and dX, dW are scaled back in fp32; this
  * needs (1 - eps) w_y + (eps/V) sum_j w_j + 2 s lse < 64 on every row (class weights below
- * ~60 in practice), else the band overflows to inf. Not a part of the pages' method, whose
+ * ~60 in practice); a row above it is reported by flce_check_device_error as
+ * FLCE_ERR_F16_RANGE (its gradient would overflow the band). Not a part of the pages' method, whose
  * kernels take 16-bit inputs ([P4] "Summary"). */
 typedef enum { FLCE_INPUT_BF16 = 0, FLCE_INPUT_F16 = 1 } flce_input_dtype;
 
@@ -235,8 +238,9 @@ flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* ta
                                 void* workspace, size_t ws_bytes, struct CUstream_st* stream);
 
 /* Synchronises `stream`, then reads and clears the device error word of the
- * most recent call that used `workspace`. Returns FLCE_OK, FLCE_ERR_BAD_TARGET,
- * FLCE_ERR_TIMEOUT, or FLCE_ERR_CUDA if the copy itself failed. */
+ * most recent call that used `workspace`. Returns FLCE_OK, FLCE_ERR_TIMEOUT,
+ * FLCE_ERR_BAD_TARGET, FLCE_ERR_F16_RANGE (in that order of precedence), or
+ * FLCE_ERR_CUDA if the copy itself failed. */
 flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream);
 
 /* A static, human-readable name for a status. */

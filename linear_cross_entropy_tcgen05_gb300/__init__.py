@@ -38,7 +38,7 @@ INPUT_DTYPES = {"bf16": 0, "f16": 1}  # flce_input_dtype of X, W and dX
 STATUS = {
     0: "FLCE_OK", 1: "FLCE_ERR_INVALID_ARG", 2: "FLCE_ERR_ALIGNMENT", 3: "FLCE_ERR_UNSUPPORTED_DEVICE",
     4: "FLCE_ERR_WORKSPACE_TOO_SMALL", 5: "FLCE_ERR_REDUCTION_NONE_GRAD", 6: "FLCE_ERR_CUDA",
-    7: "FLCE_ERR_BAD_TARGET", 8: "FLCE_ERR_TIMEOUT", 9: "FLCE_ERR_TOO_LARGE",
+    7: "FLCE_ERR_BAD_TARGET", 8: "FLCE_ERR_TIMEOUT", 9: "FLCE_ERR_TOO_LARGE", 10: "FLCE_ERR_F16_RANGE",
 }
 EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flce_check_device_error",
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",

@@ -343,6 +343,7 @@ const char* flce_status_string(flce_status st) {
     case FLCE_ERR_BAD_TARGET: return "FLCE_ERR_BAD_TARGET: a target outside [0, V) that is not ignore_index";
     case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT: a device pipeline wait exceeded its limit";
     case FLCE_ERR_TOO_LARGE: return "FLCE_ERR_TOO_LARGE: a size exceeds 2^30";
+    case FLCE_ERR_F16_RANGE: return "FLCE_ERR_F16_RANGE: an f16 gradient coefficient exceeds the f16 range";
   }
   return "unknown flce_status";
 }
@@ -864,6 +865,7 @@ flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream_
   FLCE_CUDA_CHECK(cudaMemset(workspace, 0, sizeof(int)));
   if (word & FLCE_DEVERR_TIMEOUT) return FLCE_ERR_TIMEOUT;
   if (word & FLCE_DEVERR_BAD_TARGET) return FLCE_ERR_BAD_TARGET;
+  if (word & FLCE_DEVERR_F16_RANGE) return FLCE_ERR_F16_RANGE;
   return FLCE_OK;
 }
 

@@ -13,6 +13,7 @@ namespace flce {
 // values by flce_check_device_error).
 constexpr int FLCE_DEVERR_BAD_TARGET = 1;
 constexpr int FLCE_DEVERR_TIMEOUT = 2;
+constexpr int FLCE_DEVERR_F16_RANGE = 4;  // a scaled f16 gradient coefficient exceeds the f16 range
 
 // Output tiles of the tensor-core GEMMs: 128 rows per CTA (TMEM lanes) x 256 columns,
 // a CTA pair owning 256 x 256; K staged 64 16-bit elements (128 bytes, one

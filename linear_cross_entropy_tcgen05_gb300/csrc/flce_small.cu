@@ -220,7 +220,10 @@ __global__ void __launch_bounds__(256) flce_coef_kernel(const PrepParams p, int 
     const float l = p.lse[i];
     const float wy = p.cw != nullptr ? __ldg(p.cw + y) : 1.f;
     const float a = g * ((1.f - p.eps) * wy + p.eps / float(p.V) * wtot + 2.f * p.zscale * l);
-    cf = make_float4(a, -l * kLog2e, g * (1.f - p.eps) * wy, __int_as_float(y - p.y_offset));
+    const float c = g * (1.f - p.eps) * wy;
+    // f16 band: the largest gradient entry of the row is below max(a, c) in magnitude
+    if (p.gscale > 0.f && !(a <= 65504.f && c <= 65504.f)) atomicOr(p.err, FLCE_DEVERR_F16_RANGE);
+    cf = make_float4(a, -l * kLog2e, c, __int_as_float(y - p.y_offset));
   }
   p.coef[i] = cf;
 }

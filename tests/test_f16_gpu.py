@@ -131,3 +131,26 @@ def test_f16_through_autograd(gpu_lib):
     assert Xa.grad.dtype == F16 and Wa.grad.dtype == F16
     assert rel_fro(Xa.grad.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
     assert rel_fro(Wa.grad.float().cpu().numpy(), ref_dW) <= 1e-2
+
+
+def test_f16_gradient_range_is_reported(gpu_lib):
+    """A class weight too large for the scaled f16 gradient band is reported, not hidden."""
+    wl = custom("f16_range", 256, 128, 1024, seed=66)
+    X, W, y = make_inputs(wl, dtype=F16)
+    cw = torch.ones(wl.V, device=DEV)
+    cw[int(y[0])] = 100.0  # (1 - eps) w_y = 100 > 64
+    N, D, V = wl.N, wl.D, wl.V
+    Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
+    ws = _ws(N, D, V, 2)
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    opts = flce.make_options(class_weight=cw, input_dtype="f16")
+    flce.flce_forward_ex(Xd, Wd, yd, loss, lse, ws, options=opts)
+    assert flce.flce_check_device_error(ws) == 0
+    dX = torch.empty(N, D, dtype=F16, device=DEV)
+    dW = torch.empty(D, V, device=DEV)
+    flce.flce_backward_ex(Xd, Wd, yd, lse, torch.ones(1, device=DEV), dX, dW, ws, options=opts)
+    assert flce.STATUS[flce.flce_check_device_error(ws)] == "FLCE_ERR_F16_RANGE"
+    # weights in range pass
+    cw[int(y[0])] = 50.0
+    flce.flce_backward_ex(Xd, Wd, yd, lse, torch.ones(1, device=DEV), dX, dW, ws, options=opts)
+    assert flce.flce_check_device_error(ws) == 0

@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // G = A exp2(u log2e - lse log2e) - B w_j - [col == y] C (times 1 - (u/c)^2 with a
         // softcap), zero outside the vocabulary and on ignored rows.
         const int row = t.a_row + r;
-        float4 cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
+        float4 cf = make_float4(0.f, -CUDART_INF_F, 0.f, __int_as_float(kIgnoredRow));
         if (row < gp.N) cf = __ldg(gp.coef + row);
         const int y = __float_as_int(cf.w);
         const float brow = (y == kIgnoredRow) ? 0.f : __ldg(gp.bval);

@@ -212,7 +212,9 @@ __global__ void __launch_bounds__(256) flce_coef_kernel(const PrepParams p, int 
   const int y = p.targets[i];
   float4 cf;
   if (y == p.ignore_index) {
-    cf = make_float4(0.f, 0.f, 0.f, __int_as_float(kIgnoredRow));
+    // A = 0 and an exponent of -inf: the epilogue's A * exp2(u log2e + y) is exactly 0 for
+    // any logit u (with y = 0 a logit above ~88 would give 0 * inf = NaN)
+    cf = make_float4(0.f, -CUDART_INF_F, 0.f, __int_as_float(kIgnoredRow));
   } else if (y < 0 || y >= p.V) {
     atomicOr(p.err, FLCE_DEVERR_BAD_TARGET);
     cf = make_float4(CUDART_NAN_F, 0.f, 0.f, __int_as_float(kIgnoredRow));

@@ -146,3 +146,47 @@ def test_autograd_wrapper(gpu_lib):
     assert abs(loss.item() - ref_loss) <= TOL_LOSS_REL * abs(ref_loss)
     assert rel_fro(Xd.grad.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
     assert rel_fro(Wd.grad.float().cpu().numpy(), ref_dW) <= 1e-2  # dW returned in bf16 through autograd
+
+
+def test_zero_weights_give_the_closed_form(gpu_lib):
+    """W = 0: every logit is 0, lse = ln V, loss = ln V + s (ln V)^2, dX = 0 and
+    dZ = g (p (1 + 2 s lse) - (1 - eps) onehot - eps/V) with p = 1/V (the oracle's own pin,
+    here on the GPU)."""
+    import math
+    wl = custom("w0", 300, 128, 1000, seed=20, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-3)
+    X, W, y = make_inputs(wl)
+    W = torch.zeros_like(W)
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean")
+    assert run.forward() == 0
+    assert run.backward() == 0
+    got = run.host()
+    lnV = math.log(wl.V)
+    valid = y.numpy() != wl.ignore_index
+    assert np.max(np.abs(got["lse"] - lnV)) <= 1e-5
+    assert abs(got["loss"][0] - (lnV + 1e-3 * lnV * lnV)) <= 1e-5
+    assert np.all(got["dX"] == 0.0)
+    _, _, _, ref_dW = oracle.forward_backward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean")
+    assert rel_fro(got["dW"], ref_dW) <= TOL_DW_REL
+    assert valid.sum() > 0
+
+
+def test_large_logits_stay_finite(gpu_lib):
+    """Logits in the hundreds (X scaled by 64): the online softmax keeps every exponent
+    <= 0, so nothing overflows, and the results still match the oracle. Ignored rows must
+    give exact zeros here too (their coefficient has an exponent of -inf, not 0: with 0,
+    exp2 of a logit above ~88 overflows and 0 * inf poisons dW with NaN)."""
+    wl = custom("big", 512, 256, 4104, seed=21, ignore_frac=0.05, label_smoothing=0.1, zloss_scale=1e-4)
+    X, W, y = make_inputs(wl)
+    X = (X.float() * 64).bfloat16()
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean")
+    assert run.forward() == 0
+    assert run.backward() == 0
+    got = run.host()
+    loss, lse, dX, dW = oracle.forward_backward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale,
+                                                "mean")
+    valid = y.numpy() != wl.ignore_index
+    assert np.isfinite(got["loss"]).all() and np.isfinite(got["dW"]).all() and np.isfinite(got["dX"]).all()
+    assert abs(got["loss"][0] - loss) <= TOL_LOSS_REL * abs(loss)
+    assert np.max(np.abs(got["lse"][valid] - lse[valid])) <= TOL_LSE_ABS
+    assert rel_fro(got["dX"], dX) <= TOL_DX_REL
+    assert rel_fro(got["dW"], dW) <= TOL_DW_REL

@@ -21,6 +21,9 @@ CASES = [
     ("vocab_32008", custom("v32008", 300, 64, 32008, seed=9, ignore_frac=0.2, label_smoothing=0.05)),
     ("zloss_mean", custom("zl", 512, 256, 2048, seed=10, zloss_scale=0.01, ignore_frac=0.3)),
     ("deep_k", custom("deepk", 256, 1032, 768, seed=11, reduction="sum")),
+    # ignore_index that is also a class id, near-total smoothing, a strong z-loss
+    ("unusual_options", custom("odd", 333, 72, 1544, seed=22, ignore_frac=0.1, ignore_index=0,
+                               label_smoothing=0.999, zloss_scale=1.0)),
 ]
 
 

@@ -158,7 +158,7 @@ def test_fp32_dx_output(gpu_lib):
     assert rel_fro(dX32.cpu().numpy(), ref_dX) <= 5e-3
 
 
-@pytest.mark.parametrize("cuts", [[0, 1000, 2048, 4104], [0, 264, 4104], [0, 4104]])
+@pytest.mark.parametrize("cuts", [[0, 1000, 2048, 4104], [0, 264, 4104], [0, 4104], [0, 8, 4096, 4104]])
 @pytest.mark.parametrize("eps,s,red", [(0.0, 0.0, "mean"), (0.1, 1e-3, "sum")])
 def test_vocabulary_shards_match_the_whole(gpu_lib, cuts, eps, s, red):
     wl = custom("shards", 700, 136, 4104, seed=35, ignore_frac=0.1)
@@ -209,7 +209,8 @@ def test_vocabulary_shards_match_the_whole(gpu_lib, cuts, eps, s, red):
         assert np.max(np.abs(st[2] - zy_k)) <= 1e-3
 
 
-@pytest.mark.parametrize("row_band,opts", [(300, {}), (256, {"cw": True}), (512, {"bias": True, "softcap": 8.0})])
+@pytest.mark.parametrize("row_band,opts", [(300, {}), (256, {"cw": True}), (512, {"bias": True, "softcap": 8.0}),
+                                            (999, {})])  # the last band holds one row
 def test_row_band_backward_matches_the_oracle(gpu_lib, row_band, opts):
     """Micro-batching along N: the backward in bands of rows, with a workspace sized for one band."""
     wl = custom("bands", 1000, 136, 4104, seed=36, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-3)

@@ -193,3 +193,21 @@ def test_large_logits_stay_finite(gpu_lib):
     assert np.max(np.abs(got["lse"][valid] - lse[valid])) <= TOL_LSE_ABS
     assert rel_fro(got["dX"], dX) <= TOL_DX_REL
     assert rel_fro(got["dW"], dW) <= TOL_DW_REL
+
+
+@pytest.mark.parametrize("where", ["first", "last"])
+def test_targets_at_the_vocabulary_edges(gpu_lib, where):
+    """Every target in column 0, or in column V-1 (inside the last, partly masked tile):
+    the one tile that holds the target captures its logit."""
+    wl = custom("edge", 300, 128, 1000, seed=23, label_smoothing=0.1)
+    X, W, y = make_inputs(wl)
+    y = torch.full_like(y, 0 if where == "first" else wl.V - 1)
+    y[::7] = IGNORE_INDEX
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing)
+    assert run.forward() == 0
+    assert run.backward() == 0
+    got = run.host()
+    loss, lse, dX, dW = oracle.forward_backward(X, W, y, wl.ignore_index, wl.label_smoothing)
+    assert abs(got["loss"][0] - loss) <= TOL_LOSS_REL * abs(loss)
+    assert rel_fro(got["dX"], dX) <= TOL_DX_REL
+    assert rel_fro(got["dW"], dW) <= TOL_DW_REL

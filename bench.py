@@ -463,12 +463,18 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
 
 
 def _kernel_hash() -> str:
+    """Hash of the GEMM kernels' source code with comments and blank space removed, so
+    that a recorded ncu traffic figure stays attached to the code it was measured on."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("flce_gemm.cu", "sm103_ptx.cuh", "flce_internal.h"):
         p = os.path.join(ROOT, "linear_cross_entropy_tcgen05_gb300", "csrc", f)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            src = open(p).read()
+            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+            src = re.sub(r"//[^\n]*", " ", src)
+            h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -26,7 +26,7 @@ __all__ = [
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
     "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail", "flce_kernel_launches",
-    "flce_selftest_wait_timeout", "flce_backward_band_width",
+    "flce_selftest_wait_timeout", "flce_backward_band_width", "FusedLinearCrossEntropyLoss",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -363,7 +363,7 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, X, W, targets, ignore_index=-100, label_smoothing=0.0, zloss_scale=0.0, reduction="mean",
-                softcap=0.0, bias=None, class_weight=None, weight_layout="dv"):
+                softcap=0.0, bias=None, class_weight=None, weight_layout="dv", metrics=None):
         layout = _layout(weight_layout)
         _validate(X, W, targets, layout)
         N, D = X.shape
@@ -373,7 +373,13 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         lse = torch.empty(N, dtype=torch.float32, device=X.device)
         b32 = bias.detach().float().contiguous() if bias is not None else None
         w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout, input_dtype=X.dtype)
+        pred = acc = None
+        if metrics is not None:  # argmax per row and token accuracy, from the same forward pass
+            pred = torch.empty(N, dtype=torch.int32, device=X.device)
+            acc = torch.empty(1, dtype=torch.float32, device=X.device)
+            metrics["predicted"], metrics["accuracy"] = pred, acc
+        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout, input_dtype=X.dtype,
+                            predicted=pred, accuracy=acc)
         flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction, opts)
         ctx.save_for_backward(X, W, targets, lse)
         ctx.extra = (b32, w32, bias is not None and bias.requires_grad, bias.dtype if bias is not None else None)
@@ -399,7 +405,7 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction,
                          opts)
         return (dX, dW.to(W.dtype), None, None, None, None, None, None,
-                db.to(b_dtype) if db is not None else None, None, None)
+                db.to(b_dtype) if db is not None else None, None, None, None)
 
 
 def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,
@@ -416,3 +422,43 @@ def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothin
     """
     return LinearCrossEntropyFunction.apply(X, W, targets, ignore_index, label_smoothing, zloss_scale, reduction,
                                             softcap, bias, class_weight, weight_layout)
+
+
+class FusedLinearCrossEntropyLoss(torch.nn.Module):
+    """The loss of a language-model head as a module: ``loss(weight, hidden, target,
+    bias=None)`` with ``weight`` the [V, D] weight of an ``nn.Linear(D, V)`` head, ``hidden``
+    [BT, D] hidden states (bf16 or f16, like the weight) and ``target`` [BT] token ids.
+
+    The options follow the feature list of Liger-Kernel PR #1291 ("Summary"): ``ce_weight``
+    (per-class weights), ``ignore_index``, ``lse_square_scale`` (z-loss), ``label_smoothing``,
+    ``reduction`` ('mean', 'sum', or 'none' for a forward without gradient), ``softcap``,
+    ``return_token_accuracy`` and ``return_predicted_tokens``. With either return flag the
+    module returns a tuple (loss, accuracy or None, predicted or None); the extra outputs
+    carry no gradient. Targets of any integer type are accepted (converted to int32).
+    """
+
+    def __init__(self, ce_weight=None, ignore_index: int = -100, lse_square_scale: float = 0.0,
+                 label_smoothing: float = 0.0, reduction: str = "mean", softcap: float | None = None,
+                 return_token_accuracy: bool = False, return_predicted_tokens: bool = False):
+        super().__init__()
+        if reduction not in REDUCTIONS:
+            raise ValueError(f"reduction must be one of {sorted(REDUCTIONS)}")
+        self.ce_weight = ce_weight
+        self.ignore_index = int(ignore_index)
+        self.lse_square_scale = float(lse_square_scale)
+        self.label_smoothing = float(label_smoothing)
+        self.reduction = reduction
+        self.softcap = float(softcap or 0.0)
+        self.return_token_accuracy = bool(return_token_accuracy)
+        self.return_predicted_tokens = bool(return_predicted_tokens)
+
+    def forward(self, weight, hidden, target, bias=None):
+        metrics = {} if (self.return_token_accuracy or self.return_predicted_tokens) else None
+        loss = LinearCrossEntropyFunction.apply(
+            hidden, weight, target.to(torch.int32).contiguous(), self.ignore_index, self.label_smoothing,
+            self.lse_square_scale, self.reduction, self.softcap, bias, self.ce_weight, "vd", metrics)
+        if metrics is None:
+            return loss
+        acc = metrics["accuracy"][0] if self.return_token_accuracy else None
+        pred = metrics["predicted"] if self.return_predicted_tokens else None
+        return loss, acc, pred

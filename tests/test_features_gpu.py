@@ -308,3 +308,28 @@ def test_gradient_accumulation_over_micro_batches(gpu_lib):
     torch.cuda.synchronize()
     assert rel_fro(dW.cpu().numpy(), dW1.cpu().numpy()) <= 1e-5
     assert rel_fro(db.cpu().numpy(), db1.cpu().numpy()) <= 1e-5
+
+
+def test_loss_module_with_metrics(gpu_lib):
+    """FusedLinearCrossEntropyLoss on an nn.Linear-layout weight: the loss and gradients of
+    the autograd path, plus token accuracy and predictions from the same forward."""
+    wl = custom("module", 640, 136, 3000, seed=39, ignore_frac=0.1, label_smoothing=0.05, zloss_scale=1e-4)
+    X, W, y, bias, cw = _inputs(wl)
+    head = W.t().contiguous().to(DEV).requires_grad_()   # [V, D]
+    hidden = X.to(DEV).requires_grad_()
+    b = bias.to(DEV).requires_grad_()
+    crit = flce.FusedLinearCrossEntropyLoss(ce_weight=cw.to(DEV), ignore_index=wl.ignore_index,
+                                            lse_square_scale=wl.zloss_scale, label_smoothing=wl.label_smoothing,
+                                            softcap=12.0, return_token_accuracy=True, return_predicted_tokens=True)
+    loss, acc, pred = crit(head, hidden, y.to(DEV).long(), b)
+    loss.backward()
+    torch.cuda.synchronize()
+    ref_loss, _, ref_dX, ref_dW, ref_db = oracle.forward_backward_ext(
+        X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean", softcap=12.0, bias=bias,
+        class_weight=cw)
+    assert abs(loss.item() - ref_loss) <= TOL_LOSS_REL * abs(ref_loss)
+    assert rel_fro(hidden.grad.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
+    assert rel_fro(head.grad.float().cpu().numpy().T, ref_dW) <= 1e-2   # returned in bf16
+    assert rel_fro(b.grad.float().cpu().numpy(), ref_db) <= TOL_DW_REL
+    valid = y.numpy() != IGNORE_INDEX
+    _check_argmax(pred.cpu().numpy(), X, W, y.numpy(), bias, 12.0, valid, acc.item())

@@ -241,3 +241,15 @@ def test_fused_workspace_is_the_larger_of_the_two():
         f = flce.flce_workspace_size(n, d, v, 0)
         b = flce.flce_workspace_size(n, d, v, 1)
         assert flce.flce_workspace_size(n, d, v, 2) == max(f, b)
+
+
+def test_loss_module_checks_its_arguments():
+    with pytest.raises(ValueError, match="reduction"):
+        flce.FusedLinearCrossEntropyLoss(reduction="avg")
+    crit = flce.FusedLinearCrossEntropyLoss(return_predicted_tokens=True)
+    weight = torch.zeros(16, 8, dtype=torch.bfloat16)     # [V, D]
+    hidden = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        crit(weight, hidden, torch.zeros(4, dtype=torch.int64))   # shapes fine, CPU tensors refused
+    with pytest.raises(ValueError, match=r"W \[V,D\]"):
+        crit(weight.t().contiguous(), hidden, torch.zeros(4, dtype=torch.int64))

@@ -43,6 +43,9 @@ namespace {
 #ifndef FLCE_DW_TRANSPOSE_ODD
 #define FLCE_DW_TRANSPOSE_ODD 1  // 1: G^T X with a transposed store when D's row tiles are odd
 #endif
+#ifndef FLCE_L2_PROMOTION
+#define FLCE_L2_PROMOTION 3  // tensor-map L2 promotion: 0 none, 1 64 B, 2 128 B, 3 256 B
+#endif
 #ifndef FLCE_FWD_GN
 #define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
 #endif
@@ -260,7 +263,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const voi
   const cuuint32_t es[2] = {1, 1};
   return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  static_cast<CUtensorMapL2promotion>(FLCE_L2_PROMOTION),
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS ||
          (note_error("cuTensorMapEncodeTiled", "the tensor map was refused"), false);
 }

@@ -189,6 +189,23 @@ def oracle_sample_for(wl, X, W, y, seconds: float, chunk: int = 256):
     return rows / dt, rows, dt
 
 
+def pipeline_waits(ws, phase):
+    """Shares of the MMA thread's cycles spent waiting, read from the workspace header of
+    the last call, which a library built with -DFLCE_WAIT_STATS=1 fills: per GEMM kind,
+    cycles the MMA thread waited for operands (full stages) and for a drained accumulator,
+    and cycles the producer waited for a free stage, over the MMA thread's total."""
+    h = ws[:256].cpu().view(torch.int64).tolist()
+    kinds = {"forward": -1} if phase == "fwd" else {"gradient": 0, "dW": 1, "dX": 2}
+    out = {}
+    for name, k in kinds.items():
+        base = (32 + 32 * (k + 1)) // 8
+        full, tempty, empty, total = h[base:base + 4]
+        if total > 0:
+            out[name] = {"mma_waits_operands": full / total, "mma_waits_epilogue": tempty / total,
+                         "producer_waits_free_stage": empty / total}
+    return out
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -264,8 +281,12 @@ def run_ours(args, wl, world, rank, local):
         for _ in range(args.warmup + args.steps):
             step()
         torch.cuda.synchronize(dev)
+        line = {"only": args.only, "workload": wl.name}
+        if args.wait_stats:
+            line["pipeline_waits"] = pipeline_waits(ws, args.only)
         st = flce.flce_check_device_error(ws, stream)
-        print(json.dumps({"only": args.only, "workload": wl.name, "status": flce.flce_status_string(st)}))
+        line["status"] = flce.flce_status_string(st)
+        print(json.dumps(line))
         if st != 0:
             raise SystemExit(1)
         return
@@ -490,6 +511,8 @@ def main():
     ap.add_argument("--shape", default=None, help="N,D,V override of the workload's shape (profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--wait-stats", action="store_true",
+                    help="with --only and a library built with -DFLCE_WAIT_STATS=1: print pipeline wait shares")
     ap.add_argument("--only", choices=["fwd", "bwd"], default=None,
                     help="profiling driver: run only this phase (warm-up + steps), print a status line")
     args = ap.parse_args()

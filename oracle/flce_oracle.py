@@ -5,8 +5,8 @@ TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 this module. The CUDA library never does, and the two share no code: the oracle
 takes its inputs as plain arrays from the seeded generators in ``workloads``.
 
-It works on the same bf16-rounded inputs as the GPU path, widened exactly to
-float64, and computes everything in float64 with numpy. Matrix products use
+It works on the same bf16-rounded (or f16-rounded) inputs as the GPU path, widened
+exactly to float64, and computes everything in float64 with numpy. Matrix products use
 numpy's ``@`` as a library step; there is no blocking or fusion beyond splitting
 independent rows into batches to bound memory.
 
@@ -39,7 +39,8 @@ design notes):
 * a target outside [0, V) that is not the ignore index has no defined loss: that
   row's loss and gradient are NaN.
 
-Every function here has a pin in ``tests/test_oracle_pins.py`` (closed forms,
+Every function here has a pin in ``tests/test_oracle_pins.py`` or, for the
+extended options and shards, ``tests/test_oracle_ext_pins.py`` (closed forms,
 invariants, brute force, a torch fp64 library routine and central finite
 differences); none is "parity unpinned".
 """

@@ -8,12 +8,14 @@
 //   2. finalize: combine the partials -> lse, row losses, deterministic reduction.
 // Backward ("Backward Pass" and "Path to Production" of the same post; PR #1291: dW
 //           contracts over the tokens and is written once):
-//   1. prep: number of valid rows, g, per-row coefficients;
-//   2. for every band of Vc vocabulary columns:
-//        gradient GEMM : recompute the logits, G = dZ in bf16 into the band;
-//        dW GEMM       : dW[:, band] = X^T G   (K = N, each block written once);
+//   1. prep: number of valid rows, g (over the whole batch), per-row coefficients;
+//   2. for every band of Vc vocabulary columns (Vc picked so that the dW launches fill
+//      whole waves of resident clusters), and for every row band when row_band is set:
+//        gradient GEMM : recompute the logits, G = dZ in bf16 (f16: scaled) into the band;
+//        dW GEMM       : dW[:, band] = X^T G   (K = rows, each block written once; later
+//                        row bands, or accumulate_grads, add into it);
 //        dX GEMM       : dX_acc (+)= G W[:, band]^T (fp32, TMA element-wise add);
-//   3. cast dX_acc to bf16.
+//   3. cast dX_acc to bf16 (or f16), unless the caller asked for the fp32 dX.
 #include <cmath>
 #include <cstdio>
 #include <cstring>

@@ -156,8 +156,11 @@ typedef enum { FLCE_WEIGHT_DV = 0, FLCE_WEIGHT_VD = 1 } flce_weight_layout;
  * probabilities near 1/V stay normal f16 numbers) and dX, dW are scaled back in fp32; this
  * needs (1 - eps) w_y + (eps/V) sum_j w_j + 2 s lse < 64 on every row (class weights below
  * ~60 in practice); a row above it is reported by flce_check_device_error as
- * FLCE_ERR_F16_RANGE (its gradient would overflow the band). Not a part of the pages' method, whose
- * kernels take 16-bit inputs ([P4] "Summary"). */
+ * FLCE_ERR_F16_RANGE (its gradient would overflow the band). dX is rounded once from its
+ * fp32 accumulator to f16, so entries below f16's normal range (6.1e-5) keep only
+ * absolute precision: scale the loss (grad_out) or ask for the fp32 dX (dX_f32) when
+ * gradients are that small. Not a part of the pages' method, whose kernels take 16-bit
+ * inputs ([P4] "Summary"). */
 typedef enum { FLCE_INPUT_BF16 = 0, FLCE_INPUT_F16 = 1 } flce_input_dtype;
 
 typedef struct flce_options {

@@ -36,7 +36,14 @@ def _case(i):
     )
 
 
-CASES = [_case(i) for i in range(24)]
+CASES = [_case(i) for i in range(24)] + [
+    # f16 with heavy smoothing and a small grad_out: dX entries near 1e-6, below f16's
+    # normal range, so the f16 output itself carries percent-level rounding error
+    dict(N=972, D=1720, V=4432, seed=60021, ignore_frac=0.05, eps=0.9, s=0.0, red="mean", layout="vd",
+         dtype="f16", softcap=5.0, bias=False, cw=True, row_band=0, grad_out=-0.25),
+    dict(N=2994, D=408, V=5944, seed=60068, ignore_frac=0.0, eps=0.9, s=0.1, red="mean", layout="dv",
+         dtype="f16", softcap=0.0, bias=False, cw=False, row_band=0, grad_out=-0.25),
+]
 
 
 @pytest.mark.parametrize("c", CASES, ids=[f"{c['N']}x{c['D']}x{c['V']}-{c['layout']}-{c['dtype']}" for c in CASES])
@@ -81,7 +88,10 @@ def test_random_case_matches_the_oracle(gpu_lib, c):
     if valid.any():
         assert np.max(np.abs(lse.cpu().double().numpy()[valid] - ref_lse[valid])) <= TOL_LSE_ABS
     dWn = dW.cpu().numpy()
-    assert rel_fro(dX.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
+    # dX is rounded once to X's type; its own rounding of the exact dX (large where entries
+    # fall below f16's normal range, 6.1e-5) is added to the tolerance
+    fmt_err = rel_fro(torch.from_numpy(ref_dX).to(dt).double().numpy(), ref_dX)
+    assert rel_fro(dX.float().cpu().numpy(), ref_dX) <= TOL_DX_REL + fmt_err
     assert rel_fro(dWn.T if c["layout"] == "vd" else dWn, ref_dW) <= TOL_DW_REL
     if bias is not None:
         assert rel_fro(db.cpu().numpy(), ref_db) <= TOL_DW_REL

@@ -96,3 +96,71 @@ def test_random_case_matches_the_oracle(gpu_lib, c):
     if bias is not None:
         assert rel_fro(db.cpu().numpy(), ref_db) <= TOL_DW_REL
     assert np.all(dX.float().cpu().numpy()[~valid] == 0.0)
+
+
+def _shard_case(i):
+    g = np.random.default_rng(90000 + i)
+    N = int(g.integers(1, 1200))
+    D = 8 * int(g.integers(1, 100))
+    V = 8 * int(g.integers(2, 1500))
+    K = int(g.integers(1, 4))
+    cuts = sorted(set([0, V] + [8 * int(x) for x in g.integers(1, V // 8, size=K - 1)]))
+    return dict(N=N, D=D, V=V, cuts=cuts, seed=91000 + i, ignore_frac=float(g.choice([0.0, 0.2])),
+                eps=float(g.choice([0.0, 0.1])), s=float(g.choice([0.0, 1e-3])), red=str(g.choice(["mean", "sum"])),
+                layout=str(g.choice(["dv", "vd"])), dtype="f16" if g.random() < 0.3 else "bf16")
+
+
+SHARD_CASES = [_shard_case(i) for i in range(8)]
+
+
+@pytest.mark.parametrize("c", SHARD_CASES, ids=[f"{c['N']}x{c['D']}x{c['V']}-{len(c['cuts']) - 1}shards"
+                                                for c in SHARD_CASES])
+def test_random_vocabulary_shards(gpu_lib, c):
+    """Random splits of the vocabulary: shard statistics, their combination and the shard
+    backward reproduce the whole-vocabulary oracle."""
+    dt = torch.float16 if c["dtype"] == "f16" else torch.bfloat16
+    wl = custom("sh", c["N"], c["D"], c["V"], seed=c["seed"], ignore_frac=c["ignore_frac"])
+    X, W, y = make_inputs(wl, dtype=dt)
+    N, D, V = wl.N, wl.D, wl.V
+    Xd, yd = X.to(DEV), y.to(DEV)
+
+    def ws(n, d, v, which):
+        return torch.empty(flce.flce_workspace_size(n, d, v, which), dtype=torch.uint8, device=DEV)
+
+    opt = flce.make_options(weight_layout=c["layout"], input_dtype=dt)
+    cuts = c["cuts"]
+    stats = torch.empty(len(cuts) - 1, 4, N, device=DEV)
+    shards = []
+    for k, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        Wk = (W[:, a:b].t() if c["layout"] == "vd" else W[:, a:b]).contiguous().to(DEV)
+        shards.append((a, b, Wk))
+        w_ = ws(N, D, b - a, 0)
+        flce.flce_shard_stats(Xd, Wk, yd, a, stats[k], w_, options=opt)
+        assert flce.flce_check_device_error(w_) == 0
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    wc = ws(N, 8, 8, 0)
+    flce.flce_combine_shards(stats, yd, V, loss, lse, wc, label_smoothing=c["eps"], zloss_scale=c["s"],
+                             reduction=c["red"])
+    assert flce.flce_check_device_error(wc) == 0
+    dX = torch.zeros(N, D, device=DEV)
+    dW = torch.empty(D, V, device=DEV)
+    for a, b, Wk in shards:
+        part = torch.empty(N, D, device=DEV)
+        dWk = torch.empty(tuple(Wk.shape), device=DEV)
+        w_ = ws(N, D, b - a, 1)
+        flce.flce_backward_ex(Xd, Wk, yd, lse, torch.ones(1, device=DEV), None, dWk, w_,
+                              label_smoothing=c["eps"], zloss_scale=c["s"], reduction=c["red"],
+                              options=flce.make_options(dX_f32=part, v_offset=a, v_total=V,
+                                                        weight_layout=c["layout"], input_dtype=dt))
+        assert flce.flce_check_device_error(w_) == 0
+        dX += part
+        dW[:, a:b] = dWk.t() if c["layout"] == "vd" else dWk
+    torch.cuda.synchronize()
+    ref_loss, ref_lse, ref_dX, ref_dW = oracle.forward_backward(X, W, y, IGNORE_INDEX, c["eps"], c["s"], c["red"])
+    valid = y.numpy() != IGNORE_INDEX
+    if abs(ref_loss) > 0:
+        assert abs(loss.item() - ref_loss) <= TOL_LOSS_REL * abs(ref_loss) + 1e-6
+    if valid.any():
+        assert np.max(np.abs(lse.cpu().double().numpy()[valid] - ref_lse[valid])) <= TOL_LSE_ABS
+    assert rel_fro(dX.cpu().numpy(), ref_dX) <= 5e-3
+    assert rel_fro(dW.cpu().numpy(), ref_dW) <= TOL_DW_REL

@@ -253,3 +253,23 @@ def test_loss_module_checks_its_arguments():
         crit(weight, hidden, torch.zeros(4, dtype=torch.int64))   # shapes fine, CPU tensors refused
     with pytest.raises(ValueError, match=r"W \[V,D\]"):
         crit(weight.t().contiguous(), hidden, torch.zeros(4, dtype=torch.int64))
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """include/flce.h is plain C: a C99 client builds with -Wall -Wextra -pedantic, links
+    against libflce.so and gets answers that need no device."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "flce_c_client")
+    libdir = os.path.dirname(flce.library_path())
+    src = os.path.join(ROOT, "tests", "c", "flce_c_client.c")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        src, "-L", libdir, "-lflce", "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split("\n")
+    version, ws, status = out[0].split()
+    assert int(version) == flce.flce_version()
+    assert int(ws) == flce.flce_workspace_size(256, 128, 1024, True)
+    assert int(status) == 1                    # FLCE_ERR_INVALID_ARG
+    assert out[1].startswith("FLCE_ERR_F16_RANGE")

@@ -60,6 +60,10 @@
  * Requirements: a compute capability 10.3 device (GB300); D % 8 == 0 and
  * V % 8 == 0 (16-byte row strides for the tensor-memory-access unit); X, W, dX,
  * dW and the workspace 16-byte aligned; targets, lse and loss 4-byte aligned.
+ * Every buffer, workspace and option array included, is device memory of the
+ * current device or managed memory: host memory (pinned or pageable) and another
+ * device's memory are refused with FLCE_ERR_INVALID_ARG before anything is
+ * launched, and flce_last_error_detail names the buffer.
  */
 #ifndef FLCE_H_
 #define FLCE_H_
@@ -75,7 +79,8 @@ struct CUstream_st; /* cudaStream_t is `struct CUstream_st *`; NULL means the le
 
 typedef enum {
   FLCE_OK = 0,
-  FLCE_ERR_INVALID_ARG = 1,          /* null pointer, size < 1, eps outside [0,1), s < 0, bad enum */
+  FLCE_ERR_INVALID_ARG = 1,          /* null pointer, size < 1, eps outside [0,1), s < 0, bad enum,
+                                        a buffer that is not memory of the current device */
   FLCE_ERR_ALIGNMENT = 2,            /* D or V not a multiple of 8, or a misaligned pointer */
   FLCE_ERR_UNSUPPORTED_DEVICE = 3,   /* the current device is not compute capability 10.3 */
   FLCE_ERR_WORKSPACE_TOO_SMALL = 4,  /* ws_bytes < flce_workspace_size(...) */
@@ -256,7 +261,9 @@ int flce_version(void);
 
 /* Which call failed the last time an entry point returned FLCE_ERR_CUDA on the calling
  * thread: the CUDA runtime or driver call and its error name, e.g.
- * "cudaMemsetAsync(...): cudaErrorInvalidValue". Empty if that never happened on this
+ * "cudaMemsetAsync(...): cudaErrorInvalidValue"; or, after FLCE_ERR_INVALID_ARG for a
+ * buffer outside the current device's memory, that buffer's name and why, e.g.
+ * "X: is host memory, not device memory". Empty if that never happened on this
  * thread; later successful calls do not clear it. The string is thread-local, owned by
  * the library and valid until the thread's next library call. Diagnostics only: the
  * pages have no counterpart. */

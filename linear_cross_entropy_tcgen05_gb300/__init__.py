@@ -354,6 +354,8 @@ def _validate(X, W, targets, layout=0):
                          + ", targets [N]")
     if not (X.is_cuda and W.is_cuda and targets.is_cuda):
         raise ValueError("X, W and targets must be CUDA tensors")
+    if not (W.device == X.device and targets.device == X.device):
+        raise ValueError("X, W and targets must be on the same device")
     if not (X.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
         raise ValueError("X, W and targets must be contiguous")
 
@@ -366,46 +368,51 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
                 softcap=0.0, bias=None, class_weight=None, weight_layout="dv", metrics=None):
         layout = _layout(weight_layout)
         _validate(X, W, targets, layout)
-        N, D = X.shape
-        V = W.shape[0] if layout == 1 else W.shape[1]
-        ws = _workspace(N, D, V, X.device, False)
-        loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
-        lse = torch.empty(N, dtype=torch.float32, device=X.device)
-        b32 = bias.detach().float().contiguous() if bias is not None else None
-        w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
-        pred = acc = None
-        if metrics is not None:  # argmax per row and token accuracy, from the same forward pass
-            pred = torch.empty(N, dtype=torch.int32, device=X.device)
-            acc = torch.empty(1, dtype=torch.float32, device=X.device)
-            metrics["predicted"], metrics["accuracy"] = pred, acc
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout, input_dtype=X.dtype,
-                            predicted=pred, accuracy=acc)
-        flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction, opts)
-        ctx.save_for_backward(X, W, targets, lse)
-        ctx.extra = (b32, w32, bias is not None and bias.requires_grad, bias.dtype if bias is not None else None)
-        ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout)
-        return loss if reduction == "none" else loss[0]
+        # the library works on the current device and the current stream: make them X's
+        with torch.cuda.device(X.device):
+            N, D = X.shape
+            V = W.shape[0] if layout == 1 else W.shape[1]
+            ws = _workspace(N, D, V, X.device, False)
+            loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
+            lse = torch.empty(N, dtype=torch.float32, device=X.device)
+            b32 = bias.detach().float().contiguous() if bias is not None else None
+            w32 = class_weight.detach().float().contiguous() if class_weight is not None else None
+            pred = acc = None
+            if metrics is not None:  # argmax per row and token accuracy, from the same forward pass
+                pred = torch.empty(N, dtype=torch.int32, device=X.device)
+                acc = torch.empty(1, dtype=torch.float32, device=X.device)
+                metrics["predicted"], metrics["accuracy"] = pred, acc
+            opts = make_options(softcap=softcap, bias=b32, class_weight=w32, weight_layout=layout,
+                                input_dtype=X.dtype, predicted=pred, accuracy=acc)
+            flce_forward_ex(X, W, targets, loss, lse, ws, ignore_index, label_smoothing, zloss_scale, reduction,
+                            opts)
+            ctx.save_for_backward(X, W, targets, lse)
+            ctx.extra = (b32, w32, bias is not None and bias.requires_grad,
+                         bias.dtype if bias is not None else None)
+            ctx.opts = (ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout)
+            return loss if reduction == "none" else loss[0]
 
     @staticmethod
     def backward(ctx, grad_loss):
         X, W, targets, lse = ctx.saved_tensors
-        b32, w32, want_db, b_dtype = ctx.extra
-        ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout = ctx.opts
-        if reduction == "none":
-            raise RuntimeError("reduction='none' has no fused backward (FLCE_ERR_REDUCTION_NONE_GRAD)")
-        N, D = X.shape
-        V = W.shape[0] if layout == 1 else W.shape[1]
-        ws = _workspace(N, D, V, X.device, True)
-        g = grad_loss.detach().to(device=X.device, dtype=torch.float32).reshape(1).contiguous()
-        dX = torch.empty_like(X)
-        dW = torch.empty(W.shape, dtype=torch.float32, device=X.device)
-        db = torch.empty(V, dtype=torch.float32, device=X.device) if want_db else None
-        opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db, weight_layout=layout,
-                            input_dtype=X.dtype)
-        flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale, reduction,
-                         opts)
-        return (dX, dW.to(W.dtype), None, None, None, None, None, None,
-                db.to(b_dtype) if db is not None else None, None, None, None)
+        with torch.cuda.device(X.device):
+            b32, w32, want_db, b_dtype = ctx.extra
+            ignore_index, label_smoothing, zloss_scale, reduction, softcap, layout = ctx.opts
+            if reduction == "none":
+                raise RuntimeError("reduction='none' has no fused backward (FLCE_ERR_REDUCTION_NONE_GRAD)")
+            N, D = X.shape
+            V = W.shape[0] if layout == 1 else W.shape[1]
+            ws = _workspace(N, D, V, X.device, True)
+            g = grad_loss.detach().to(device=X.device, dtype=torch.float32).reshape(1).contiguous()
+            dX = torch.empty_like(X)
+            dW = torch.empty(W.shape, dtype=torch.float32, device=X.device)
+            db = torch.empty(V, dtype=torch.float32, device=X.device) if want_db else None
+            opts = make_options(softcap=softcap, bias=b32, class_weight=w32, dbias=db, weight_layout=layout,
+                                input_dtype=X.dtype)
+            flce_backward_ex(X, W, targets, lse, g, dX, dW, ws, ignore_index, label_smoothing, zloss_scale,
+                             reduction, opts)
+            return (dX, dW.to(W.dtype), None, None, None, None, None, None,
+                    db.to(b_dtype) if db is not None else None, None, None, None)
 
 
 def linear_cross_entropy(X, W, targets, ignore_index: int = -100, label_smoothing: float = 0.0,

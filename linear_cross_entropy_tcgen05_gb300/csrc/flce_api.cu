@@ -19,6 +19,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -211,7 +212,7 @@ struct DevInfo {
 DevInfo g_dev[64];
 std::mutex g_dev_mu;
 
-flce_status current_device(int* sms) {
+flce_status current_device(int* sms, int* dev_out = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
@@ -231,6 +232,7 @@ flce_status current_device(int* sms) {
   }
   if (!g_dev[dev].ok) return FLCE_ERR_UNSUPPORTED_DEVICE;
   *sms = g_dev[dev].sms;
+  if (dev_out) *dev_out = dev;
   std::call_once(g_encode_once, [] {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(driver_entry("cuTensorMapEncodeTiled", 12000));
     g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_entry("cuCtxGetCurrent", 4000));
@@ -253,6 +255,43 @@ flce_status current_device(int* sms) {
     }
   }
   return FLCE_OK;
+}
+
+// Every buffer an entry point is given must be memory that device `dev` addresses as its
+// own: device memory of that device, or managed memory. Host memory (pinned or pageable)
+// and another device's memory are refused before anything is launched, since a kernel or
+// a tensor-map copy on such an address would read over the host link or fault.
+struct NamedPtr {
+  const char* name;
+  const void* p;
+};
+
+flce_status check_device_memory(int dev, std::initializer_list<NamedPtr> bufs) {
+  for (const NamedPtr& b : bufs) {
+    if (!b.p) continue;
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, b.p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      note_error(b.name, "memory kind unreadable (cudaPointerGetAttributes)");
+      return FLCE_ERR_INVALID_ARG;
+    }
+    if (a.type == cudaMemoryTypeManaged || (a.type == cudaMemoryTypeDevice && a.device == dev)) continue;
+    note_error(b.name, a.type == cudaMemoryTypeDevice ? "is memory of another device than the current one"
+                                                      : "is host memory, not device memory");
+    return FLCE_ERR_INVALID_ARG;
+  }
+  return FLCE_OK;
+}
+
+flce_status check_option_memory(int dev, const flce_options* o) {
+  if (!o) return FLCE_OK;
+  return check_device_memory(dev, {{"options.bias", o->bias},
+                                   {"options.class_weight", o->class_weight},
+                                   {"options.predicted", o->predicted},
+                                   {"options.accuracy", o->accuracy},
+                                   {"options.dbias", o->dbias},
+                                   {"options.dX_f32", o->dX_f32}});
 }
 
 // 2-D row-major tensor [outer][inner] with row pitch `pitch_elems`, 128-byte swizzled boxes.
@@ -327,9 +366,10 @@ flce_status flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, struct 
   if (!workspace) return FLCE_ERR_INVALID_ARG;
   if (!aligned(workspace, 16)) return FLCE_ERR_ALIGNMENT;
   if (ws_bytes < kHeaderBytes) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  flce_status st = current_device(&sms);
+  int sms = 0, dev = -1;
+  flce_status st = current_device(&sms, &dev);
   if (st != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"workspace", workspace}})) != FLCE_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   FLCE_CUDA_CHECK(cudaMemsetAsync(workspace, 0, kHeaderBytes, stream));
   FLCE_CUDA_CHECK(launch_wait_selftest(reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + kHdrErr), stream));
@@ -702,8 +742,12 @@ flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets
   if ((st = check_forward_outputs(loss, lse)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, false)) != FLCE_OK) return st;
   if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  int sms = 0, dev = -1;
+  if ((st = current_device(&sms, &dev)) != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"X", X}, {"W", W}, {"targets", targets}, {"workspace", workspace},
+                                      {"loss", loss}, {"lse", lse}})) != FLCE_OK ||
+      (st = check_option_memory(dev, opt)) != FLCE_OK)
+    return st;
   const int units = forward_max_units();
   if (units <= 0) {
     note_error("forward_max_units", "no resident cluster");
@@ -731,8 +775,12 @@ flce_status flce_backward_ex(const void* X, const void* W, const int32_t* target
   if ((st = check_backward_outputs(pb, opt, lse, grad_out, dX, dW)) != FLCE_OK) return st;
   if ((st = check_options(opt, pb, true)) != FLCE_OK) return st;
   if (ws_bytes < bwd_layout(backward_rows(opt, N), D, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  int sms = 0, dev = -1;
+  if ((st = current_device(&sms, &dev)) != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"X", X}, {"W", W}, {"targets", targets}, {"workspace", workspace},
+                                      {"lse", lse}, {"grad_out", grad_out}, {"dX", dX}, {"dW", dW}})) != FLCE_OK ||
+      (st = check_option_memory(dev, opt)) != FLCE_OK)
+    return st;
   return run_backward(pb, opt, lse, grad_out, dX, dW, static_cast<uint8_t*>(workspace), true, sms,
                       reinterpret_cast<cudaStream_t>(stream));
 }
@@ -761,8 +809,13 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
     const size_t f = fwd_layout(N, V).total, b = bwd_layout(backward_rows(opt, N), D, V).total;
     if (ws_bytes < (f > b ? f : b)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   }
-  int sms = 0;
-  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  int sms = 0, dev = -1;
+  if ((st = current_device(&sms, &dev)) != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"X", X}, {"W", W}, {"targets", targets}, {"workspace", workspace},
+                                      {"grad_out", grad_out}, {"loss", loss}, {"lse", lse}, {"dX", dX},
+                                      {"dW", dW}})) != FLCE_OK ||
+      (st = check_option_memory(dev, opt)) != FLCE_OK)
+    return st;
   const int units = forward_max_units();
   if (units <= 0) {
     note_error("forward_max_units", "no resident cluster");
@@ -799,8 +852,11 @@ flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* tar
   if (v_offset < 0) return FLCE_ERR_INVALID_ARG;
   if (v_offset + V >= (int64_t(1) << 30)) return FLCE_ERR_TOO_LARGE;
   if (ws_bytes < fwd_layout(N, V).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  int sms = 0, dev = -1;
+  if ((st = current_device(&sms, &dev)) != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"X", X}, {"W", W}, {"targets", targets}, {"workspace", workspace},
+                                      {"stats", stats}})) != FLCE_OK)
+    return st;
   const int units = forward_max_units();
   if (units <= 0) {
     note_error("forward_max_units", "no resident cluster");
@@ -825,8 +881,11 @@ flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* ta
   if (!aligned(stats, 4) || !aligned(targets, 4) || !aligned(workspace, 16)) return FLCE_ERR_ALIGNMENT;
   const FwdLayout L = fwd_layout(N, 8);
   if (ws_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  if ((st = current_device(&sms)) != FLCE_OK) return st;
+  int sms = 0, dev = -1;
+  if ((st = current_device(&sms, &dev)) != FLCE_OK) return st;
+  if ((st = check_device_memory(dev, {{"stats", stats}, {"targets", targets}, {"workspace", workspace},
+                                      {"loss", loss}, {"lse", lse}})) != FLCE_OK)
+    return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, s));

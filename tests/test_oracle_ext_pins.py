@@ -148,3 +148,21 @@ def test_vocabulary_shards_combine_to_the_full_loss(cuts, eps, s):
     # every valid row's target is owned by exactly one shard
     owned = sum(st[3] for st in stats)
     assert np.all(owned[y != IGNORE_INDEX] == 1.0) and np.all(owned[y == IGNORE_INDEX] == 0.0)
+
+
+def test_targets_on_shard_boundaries():
+    """Targets in the first and the last column of every shard: each is owned by exactly one
+    shard, whose target logit it carries, and the combination equals the full loss."""
+    cuts = [0, 8, 64, 65, 100]
+    X, W, _, _, _ = _problem(12, 9, 100, 8)
+    y = np.array([a for a in cuts[:-1]] + [b - 1 for b in cuts[1:]] + [IGNORE_INDEX, 50, 99, 0])
+    stats = [oracle.shard_stats(X, W[:, a:b], y, a) for a, b in zip(cuts[:-1], cuts[1:])]
+    z = X @ W
+    for k, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        mine = (y >= a) & (y < b)
+        assert np.all(stats[k][3] == mine.astype(float))
+        assert np.max(np.abs(stats[k][2][mine] - z[mine, y[mine]])) < 1e-13
+        assert np.all(stats[k][2][~mine] == 0.0)
+    loss, lse = oracle.combine_shard_stats(stats, 100, y, label_smoothing=0.1)
+    ref_loss, ref_lse = oracle.forward(X, W, y, label_smoothing=0.1)
+    assert abs(loss - ref_loss) < 1e-12 and np.max(np.abs(lse - ref_lse)) < 1e-12

@@ -148,11 +148,12 @@ def barrier(world: int):
         dist.barrier()
 
 
-def kernel_launches_per_step(N, D, V, reduction, vc=None):
+def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
-    backward denominator + row coefficients + 3 GEMMs per vocabulary band + the dX cast.
-    vc is the band width (flce_backward_band_width on the device); without it, the
-    workspace's band capacity."""
+    backward denominator + row coefficients (+ valid-row compaction and gather) + 3 GEMMs
+    per vocabulary band + the dX cast. vc is the band width (flce_backward_band_width on
+    the device); without it, the workspace's band capacity. compact: the backward
+    compacts the valid rows (the default options with a 16-bit dX)."""
     if vc is None:
         unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
         vc = max(unit, min(16384, ((3 << 28) // (2 * N)) // unit * unit))
@@ -160,7 +161,7 @@ def kernel_launches_per_step(N, D, V, reduction, vc=None):
         vc = min(vc, half)
     bands = -(-V // vc)
     fwd = 1 + 1 + (0 if reduction == "none" else 1)
-    bwd = 2 + 3 * bands + 1
+    bwd = 2 + (2 if compact else 0) + 3 * bands + 1
     return fwd + bwd, bands, vc
 
 

@@ -8,14 +8,18 @@
 //   2. finalize: combine the partials -> lse, row losses, deterministic reduction.
 // Backward ("Backward Pass" and "Path to Production" of the same post; PR #1291: dW
 //           contracts over the tokens and is written once):
-//   1. prep: number of valid rows, g (over the whole batch), per-row coefficients;
+//   1. prep: number of valid rows, g (over the whole batch), per-row coefficients; with
+//      the default options and a 16-bit dX, the valid rows' X and coefficients are
+//      gathered to the front of the dX buffer (ignored rows have a zero gradient, so the
+//      GEMMs below skip them) and the GEMMs read the device's row count;
 //   2. for every band of Vc vocabulary columns (Vc picked so that the dW launches fill
 //      whole waves of resident clusters), and for every row band when row_band is set:
 //        gradient GEMM : recompute the logits, G = dZ in bf16 (f16: scaled) into the band;
 //        dW GEMM       : dW[:, band] = X^T G   (K = rows, each block written once; later
 //                        row bands, or accumulate_grads, add into it);
 //        dX GEMM       : dX_acc (+)= G W[:, band]^T (fp32, TMA element-wise add);
-//   3. cast dX_acc to bf16 (or f16), unless the caller asked for the fp32 dX.
+//   3. cast dX_acc to bf16 (or f16) -- back to the original rows, zeros for ignored ones,
+//      after a compaction -- unless the caller asked for the fp32 dX.
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -52,6 +56,9 @@ namespace {
 #ifndef FLCE_FWD_GN
 #define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
 #endif
+#ifndef FLCE_COMPACT_ROWS
+#define FLCE_COMPACT_ROWS 1  // 1: the backward GEMMs skip ignored rows (valid-row compaction)
+#endif
 
 constexpr size_t kHeaderBytes = 256;
 constexpr int64_t kGradBandBudget = FLCE_BAND_BYTES;
@@ -64,9 +71,10 @@ struct FwdLayout {
   int S_alloc, blocks;
 };
 
-// Header words of every workspace: [0] device error word, [16] B = g eps / V (backward),
-// [24] sum of the class weights, [28] g (backward).
-constexpr size_t kHdrErr = 0, kHdrB = 16, kHdrWtot = 24, kHdrG = 28;
+// Header words of every workspace: [0] device error word, [8] number of valid rows
+// (backward compaction), [16] B = g eps / V (backward), [24] sum of the class weights,
+// [28] g (backward).
+constexpr size_t kHdrErr = 0, kHdrNValid = 8, kHdrB = 16, kHdrWtot = 24, kHdrG = 28;
 
 FwdLayout fwd_layout(int64_t N, int64_t V) {
   FwdLayout L{};
@@ -92,7 +100,7 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 constexpr int kColsumChunks = 64;
 
 struct BwdLayout {
-  size_t coef, band, dx_acc, colsum, total;
+  size_t coef, coef_c, rows, slot, band, dx_acc, colsum, total;
   int64_t Vc;
 };
 
@@ -164,6 +172,9 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V) {
   L.Vc = band_width(N, D, V);
   size_t o = kHeaderBytes;
   L.coef = o; o += align256(size_t(N) * 16);
+  L.coef_c = o; o += align256(size_t(N) * 16);
+  L.rows = o; o += align256(size_t(N) * sizeof(int));
+  L.slot = o; o += align256(size_t(N) * sizeof(int));
   L.band = o; o += align256(size_t(N) * size_t(L.Vc) * 2);
   L.dx_acc = o; o += align256(size_t(N) * size_t(D) * sizeof(float));
   L.colsum = o; o += align256(size_t(kColsumChunks) * size_t(L.Vc) * sizeof(float));
@@ -540,6 +551,25 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   return FLCE_OK;
 }
 
+bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+  if (!a || !b) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + b_bytes && y < x + a_bytes;
+}
+
+// The valid-row compaction keeps its copy of X's valid rows in the caller's 16-bit dX
+// buffer, which the backward otherwise writes only at its end: that buffer must not
+// overlap anything the backward reads.
+bool dx_free_for_scratch(const Problem& pb, const flce_options* opt, const float* lse, const float* grad_out,
+                         const void* dX) {
+  const size_t n = size_t(pb.N), d = size_t(pb.D), v = size_t(pb.V);
+  const size_t bytes = n * d * 2;
+  return !overlaps(dX, bytes, pb.X, n * d * 2) && !overlaps(dX, bytes, pb.W, d * v * 2) &&
+         !overlaps(dX, bytes, pb.targets, n * 4) && !overlaps(dX, bytes, lse, n * 4) &&
+         !overlaps(dX, bytes, grad_out, 4) && !(opt && overlaps(dX, bytes, opt->bias, v * 4)) &&
+         !(opt && overlaps(dX, bytes, opt->class_weight, v * 4));
+}
+
 // Rows handled per backward pass: all of them, or bands of opt->row_band.
 int64_t backward_rows(const flce_options* opt, int64_t N) {
   return (opt && opt->row_band > 0 && opt->row_band < N) ? opt->row_band : N;
@@ -565,6 +595,15 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const bool ext = opt_ext_grad(opt);
   const float* out_scale = pb.f16 ? gval : nullptr;  // dW, dX = g / kF16GradScale * (f16 band GEMM)
   const bool add_grads = opt && opt->accumulate_grads;  // dW (and dbias) += this call's gradient
+  // Valid-row compaction: an ignored row's gradient is zero, so the GEMMs take only the
+  // valid rows (gathered into the dX buffer) -- for the whole batch at once, a 16-bit dX
+  // and no dbias (whose column sums would read the band's unused rows).
+  const bool compact = FLCE_COMPACT_ROWS && !f32_out && Nb == pb.N && !(opt && opt->dbias) &&
+                       dx_free_for_scratch(pb, opt, lse, grad_out, dX);
+  int* n_valid_dev = reinterpret_cast<int*>(ws + kHdrNValid);
+  int* rows = reinterpret_cast<int*>(ws + L.rows);
+  int* slot = reinterpret_cast<int*>(ws + L.slot);
+  float4* coef_c = reinterpret_cast<float4*>(ws + L.coef_c);
 
   // Maps that do not depend on the row band. tmWg: B of the gradient GEMM (N = vocabulary,
   // K = D); tmWx: B of the dX GEMM (N = D, K = vocabulary). Each is MN-major in one W layout
@@ -609,7 +648,9 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const int64_t d_tiles_n = cdiv(pb.D, kBN);                         // dX columns
   for (int64_t n0 = 0; n0 < pb.N; n0 += Nb) {
     const int64_t nb = (pb.N - n0 < Nb) ? pb.N - n0 : Nb;
-    const void* Xb = static_cast<const uint8_t*>(pb.X) + size_t(n0) * size_t(pb.D) * 2;
+    // the GEMMs' X: this row band of X, or its valid rows compacted into the dX buffer
+    const void* Xb = compact ? dX : static_cast<const void*>(static_cast<const uint8_t*>(pb.X) +
+                                                             size_t(n0) * size_t(pb.D) * 2);
     float* dx_dst = f32_out ? opt->dX_f32 + size_t(n0) * size_t(pb.D) : dx_acc;
     CUtensorMap tmXk, tmXmn, tmG, tmGmn, tmDX;
     const bool enc =
@@ -628,6 +669,16 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
     pb_rows.targets = pb.targets + n0;
     pb_rows.lse = lse + n0;
     FLCE_CUDA_CHECK(launch_coef(pb_rows, int(nb), stream));
+    const float4* coef_rows = coef;
+    const int* dyn = nullptr;
+    if (compact) {
+      const CompactParams cp{pb.targets, int(pb.N), pb.ignore_index, rows, slot, n_valid_dev};
+      FLCE_CUDA_CHECK(launch_compact_rows(cp, stream));
+      const GatherParams gp{pb.X, dX, coef, coef_c, rows, n_valid_dev, int(pb.N), int(pb.D)};
+      FLCE_CUDA_CHECK(launch_gather_rows(gp, sms, stream));
+      coef_rows = coef_c;
+      dyn = n_valid_dev;
+    }
 
     const int64_t n_tiles = cdiv(cdiv(nb, gemm_tile_rows()), mc);  // row-tile groups
     for (int64_t v0 = 0, band_i = 0; v0 < pb.V; v0 += Vc, ++band_i) {
@@ -639,8 +690,10 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       wg.tiles_minor = int(vt);
       wg.num_kb = int(cdiv(pb.D, kBK));
       wg.b_row_off = int(v0);
+      wg.dyn_mode = DYN_ROW_GROUPS;
+      wg.dyn_rows = dyn;
       GradEpiParams ge{};
-      ge.coef = coef;
+      ge.coef = coef_rows;
       ge.bval = bval;
       ge.N = int(nb);
       ge.V = int(pb.V);
@@ -674,6 +727,8 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       // [V, D] dW, transposed into a [D, V] one.
       WalkParams ww{};
       ww.num_kb = int(cdiv(nb, kBK));
+      ww.dyn_mode = DYN_K_ROWS;
+      ww.dyn_rows = dyn;
       StoreEpiParams sw{(n0 > 0 || add_grads) ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
       if (!dw_vocab_rows(pb.D, pb.w_vd)) {
         ww.total_tiles = int(vt * d_tiles_m);
@@ -700,10 +755,15 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       wx.tiles_minor = int(d_tiles_n);
       wx.num_kb = int(cdiv(vc, kBK));
       wx.b_k0 = int(v0);
+      wx.dyn_mode = DYN_ROW_GROUPS;
+      wx.dyn_rows = dyn;
       StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
       FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, pb.f16, stream));
     }
-    if (!f32_out) {
+    if (compact) {
+      const ScatterCastParams sc{dx_acc, dX, slot, int(pb.N), int(pb.D), pb.f16 ? 1 : 0};
+      FLCE_CUDA_CHECK(launch_scatter_cast(sc, sms, stream));
+    } else if (!f32_out) {
       void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;
       FLCE_CUDA_CHECK(launch_cast_16bit(dx_acc, dXb, size_t(nb) * size_t(pb.D), pb.f16, sms, stream));
     }

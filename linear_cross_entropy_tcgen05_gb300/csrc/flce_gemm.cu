@@ -182,6 +182,18 @@ struct WalkSched {
     step = pr.nclusters;
     rank = pr.rank;
     pair = pr.pair;
+    if (w.dyn_rows != nullptr) {
+      // compacted valid rows: every role reads the same count, so all walk the same tiles
+      const int n = *w.dyn_rows;
+      if (w.dyn_mode == DYN_ROW_GROUPS) {
+        constexpr int group_rows = Geo<CG>::kTileRows * MC;
+        const int groups = n > group_rows ? (n + group_rows - 1) / group_rows : 1;
+        if (groups < w.total_tiles / w.tiles_minor) w.total_tiles = groups * w.tiles_minor;
+      } else if (w.dyn_mode == DYN_K_ROWS) {
+        const int kb = n > kBK ? (n + kBK - 1) / kBK : 1;
+        if (kb < w.num_kb) w.num_kb = kb;
+      }
+    }
   }
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;

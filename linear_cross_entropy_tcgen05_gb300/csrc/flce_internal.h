@@ -70,6 +70,14 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 // operand rows.
 enum WalkKind : int { WALK_GRAD = 0, WALK_DW = 1, WALK_DX = 2 };
 
+// A walk whose rows are the valid rows of the batch, compacted on the device, learns
+// their count when it starts: dyn_rows points at it (written by an earlier kernel).
+enum DynRows : int {
+  DYN_NONE = 0,
+  DYN_ROW_GROUPS = 1,  // row-tile groups (col_major == 0): only those holding valid rows
+  DYN_K_ROWS = 2,      // K runs over rows: only the 64-row blocks holding valid rows
+};
+
 struct WalkParams {
   int total_tiles;   // tiles in this launch
   int tiles_minor;   // tiles along the fast-varying output dimension
@@ -78,6 +86,40 @@ struct WalkParams {
   int b_row_off;     // added to the B operand's row/column coordinate
   int col_major;     // 1: the slow index runs over output columns (all row tiles of a
                      // column in flight), 0: over row-tile groups
+  int dyn_mode;          // DynRows: how *dyn_rows bounds the walk (at least one group or block)
+  const int* dyn_rows;   // device count of valid rows, or null
+};
+
+// Rows past the valid-row count that the compacted operands hold as zeros (with an
+// ignored-row coefficient), so that the last row-tile group and K block a walk touches
+// read defined values: a multiple of every walk's row granularity (512 and 64).
+constexpr int kCompactPadRows = 1024;
+
+struct CompactParams {
+  const int32_t* targets;
+  int N;
+  int ignore_index;
+  int* rows;     // [N] original index of each valid row, in order
+  int* slot;     // [N] compacted index of each row, -1 if ignored
+  int* n_valid;  // device scalar
+};
+
+struct GatherParams {
+  const void* X;         // 16-bit [N, D]
+  void* Xc;              // 16-bit [N, D]: valid rows first, then zeros up to the padding
+  const float4* coef;    // [N] per-row gradient coefficients
+  float4* coef_c;        // [N] the same in compacted order, ignored-row values in the padding
+  const int* rows;
+  const int* n_valid;
+  int N, D;
+};
+
+struct ScatterCastParams {
+  const float* acc;   // fp32 [N, D], compacted rows
+  void* dX;           // 16-bit [N, D], original rows (zero for ignored rows)
+  const int* slot;
+  int N, D;
+  int f16;
 };
 
 // Sentinel target of an ignored row in the per-row gradient coefficients.
@@ -235,6 +277,12 @@ cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            const WalkParams& w, const StoreEpiParams& e, bool w_vd, bool f16, cudaStream_t stream);
 // fp32 -> bf16 (or f16) of n elements, n a multiple of 4.
 cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream);
+// Valid-row compaction of the backward: the list of valid rows and their count (one
+// block), the gather of their X rows and coefficients, and the final cast of the
+// compacted dX accumulator back to the original rows.
+cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t stream);
+cudaError_t launch_gather_rows(const GatherParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_scatter_cast(const ScatterCastParams& p, int num_sms, cudaStream_t stream);
 
 constexpr int kFinalizeThreads = 256;
 

@@ -1,7 +1,8 @@
 // flce_small.cu -- the bandwidth/latency-bound helper kernels of fused linear
 // cross-entropy: the forward finalize (combine the vocabulary splits into lse, form the
 // row losses, reduce them in a fixed order), the backward prep (valid-row count and
-// per-row gradient coefficients) and the fp32 -> bf16 cast of dX.
+// per-row gradient coefficients), the valid-row compaction of the backward, and the
+// fp32 -> bf16 cast of dX.
 #include <atomic>
 
 #include <cuda_bf16.h>
@@ -269,19 +270,105 @@ __global__ void __launch_bounds__(256) flce_colsum_final_kernel(const ColsumPara
   p.out[col] = p.accumulate ? p.out[col] + s : s;
 }
 
+// Four fp32 values rounded (to nearest even) to four bf16 or f16 values.
+template <bool F16>
+__device__ __forceinline__ uint2 pack4_16bit(const float4 v) {
+  if constexpr (F16) {
+    const __half2 a = __floats2half2_rn(v.x, v.y);
+    const __half2 b = __floats2half2_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
+
 template <bool F16>
 __global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
-  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
-    const float4 v = src[i];
-    if constexpr (F16) {
-      const __half2 a = __floats2half2_rn(v.x, v.y);
-      const __half2 b = __floats2half2_rn(v.z, v.w);
-      dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-    } else {
-      const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-      const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-      dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x)
+    dst[i] = pack4_16bit<F16>(src[i]);
+}
+
+// ---------------------------------------------------------------------------------
+// Valid-row compaction of the backward. An ignored row's gradient is zero, so its logits
+// need not be recomputed, nor its zero rows of dZ multiplied into dW and dX: the GEMMs
+// run on the valid rows, gathered to the front of a scratch copy of X, and the dX
+// accumulator's rows are cast back to their original places at the end.
+// ---------------------------------------------------------------------------------
+
+// One block: each thread takes a contiguous run of rows, the block scans the per-thread
+// counts of valid rows, and every thread writes its valid rows' indices in row order.
+__global__ void __launch_bounds__(1024) flce_compact_rows_kernel(const CompactParams p) {
+  __shared__ int warp_tot[32];
+  const int tid = int(threadIdx.x), lane = tid & 31, wid = tid >> 5;
+  const int per = (p.N + 1023) / 1024;
+  const int lo = min(p.N, tid * per), hi = min(p.N, lo + per);
+  int cnt = 0;
+  for (int i = lo; i < hi; ++i) cnt += p.targets[i] != p.ignore_index ? 1 : 0;
+  int inc = cnt;  // inclusive scan within the warp, then over the warps' totals
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_tot[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    int t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += v;
     }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  int pos = inc - cnt + (wid > 0 ? warp_tot[wid - 1] : 0);
+  for (int i = lo; i < hi; ++i) {
+    if (p.targets[i] != p.ignore_index) {
+      p.rows[pos] = i;
+      p.slot[i] = pos++;
+    } else {
+      p.slot[i] = -1;
+    }
+  }
+  if (tid == 1023) *p.n_valid = warp_tot[31];
+}
+
+// Row i < n_valid of the compacted operands takes X row rows[i] and its coefficients;
+// rows from n_valid to the padding end (kCompactPadRows, at least one block) are zeros
+// with ignored-row coefficients; rows past it are never read. One warp per row.
+__global__ void __launch_bounds__(256) flce_gather_rows_kernel(const GatherParams p) {
+  const int n_valid = *p.n_valid;
+  int pad_end = ((n_valid > 0 ? n_valid : 1) + kCompactPadRows - 1) / kCompactPadRows * kCompactPadRows;
+  if (pad_end > p.N) pad_end = p.N;
+  const int lane = int(threadIdx.x) & 31;
+  const int warps = int(gridDim.x) * (int(blockDim.x) >> 5);
+  const int n16 = p.D / 8;  // 16-byte chunks of a row
+  for (int i = int(blockIdx.x) * (int(blockDim.x) >> 5) + (int(threadIdx.x) >> 5); i < pad_end; i += warps) {
+    const bool valid = i < n_valid;
+    const int src = valid ? p.rows[i] : 0;
+    const uint4* from = reinterpret_cast<const uint4*>(p.X) + size_t(src) * size_t(n16);
+    uint4* to = reinterpret_cast<uint4*>(p.Xc) + size_t(i) * size_t(n16);
+    for (int c = lane; c < n16; c += 32) to[c] = valid ? from[c] : make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0)
+      p.coef_c[i] = valid ? p.coef[src] : make_float4(0.f, -CUDART_INF_F, 0.f, __int_as_float(kIgnoredRow));
+  }
+}
+
+// dX row r = the compacted accumulator's row slot[r] in 16 bits, or zeros for an ignored
+// row. One warp per row.
+template <bool F16>
+__global__ void __launch_bounds__(256) flce_scatter_cast_kernel(const ScatterCastParams p) {
+  const int lane = int(threadIdx.x) & 31;
+  const int warps = int(gridDim.x) * (int(blockDim.x) >> 5);
+  const int n4 = p.D / 4;
+  for (int r = int(blockIdx.x) * (int(blockDim.x) >> 5) + (int(threadIdx.x) >> 5); r < p.N; r += warps) {
+    const int sl = p.slot[r];
+    const float4* from = reinterpret_cast<const float4*>(p.acc) + size_t(sl < 0 ? 0 : sl) * size_t(n4);
+    uint2* to = reinterpret_cast<uint2*>(p.dX) + size_t(r) * size_t(n4);
+    for (int c = lane; c < n4; c += 32) to[c] = sl < 0 ? make_uint2(0u, 0u) : pack4_16bit<F16>(from[c]);
   }
 }
 
@@ -355,6 +442,35 @@ cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   flce_colsum_final_kernel<<<unsigned((p.cols + 255) / 256), 256, 0, stream>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t stream) {
+  flce_compact_rows_kernel<<<1, 1024, 0, stream>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+namespace {
+// warp-per-row kernels: 8 warps a block, up to 8 blocks an SM, no more blocks than rows need
+unsigned row_blocks(int rows, int num_sms) {
+  const int need = (rows + 7) / 8, cap = num_sms * 8;
+  return unsigned(need < 1 ? 1 : (need < cap ? need : cap));
+}
+}  // namespace
+
+cudaError_t launch_gather_rows(const GatherParams& p, int num_sms, cudaStream_t stream) {
+  flce_gather_rows_kernel<<<row_blocks(p.N, num_sms), 256, 0, stream>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_cast(const ScatterCastParams& p, int num_sms, cudaStream_t stream) {
+  if (p.f16)
+    flce_scatter_cast_kernel<true><<<row_blocks(p.N, num_sms), 256, 0, stream>>>(p);
+  else
+    flce_scatter_cast_kernel<false><<<row_blocks(p.N, num_sms), 256, 0, stream>>>(p);
   count_launch();
   return cudaGetLastError();
 }

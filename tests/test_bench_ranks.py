@@ -46,9 +46,11 @@ def test_two_gloo_ranks_take_the_max_time():
 def test_launch_count_matches_the_band_schedule():
     import bench
     total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean")
-    assert (bands, vc) == (21, 6144) and total == 3 + 2 + 3 * 21 + 1   # the workspace's capacity
+    assert (bands, vc) == (21, 6144) and total == 3 + 4 + 3 * 21 + 1   # the workspace's capacity
     total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608)
-    assert bands == 28 and total == 3 + 2 + 3 * 28 + 1                  # a narrower band chosen on the device
+    assert bands == 28 and total == 3 + 4 + 3 * 28 + 1                  # a narrower band chosen on the device
+    total, _, _ = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608, compact=False)
+    assert total == 3 + 2 + 3 * 28 + 1                                  # no valid-row compaction
 
 
 def test_clock_record_decides_a_remeasurement():

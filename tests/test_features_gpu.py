@@ -153,7 +153,8 @@ def test_fp32_dx_output(gpu_lib):
     flce.flce_backward_ex(Xd, Wd, yd, lse, g, None, dW2, ws, options=flce.make_options(dX_f32=dX32))
     torch.cuda.synchronize()
     assert torch.equal(dX32.bfloat16(), dX16), "bf16 dX is the fp32 accumulator rounded once"
-    assert torch.equal(dW, dW2)
+    # the bf16-dX call compacts the valid rows, so dW sums its rows in another order
+    assert rel_fro(dW.cpu().numpy(), dW2.cpu().numpy()) <= 1e-5
     _, _, ref_dX, _ = oracle.forward_backward(X, W, y)
     assert rel_fro(dX32.cpu().numpy(), ref_dX) <= 5e-3
 

@@ -127,7 +127,11 @@ flce_status flce_forward(const void* X, const void* W, const int32_t* targets,
  * tile; dW contracts over the token dimension and each dW block is written once).
  *   lse       : fp32 [N] from flce_forward with the same inputs.
  *   grad_out  : device fp32 scalar, the upstream gradient of the reduced loss.
- *   dX        : out, bf16 [N, D] (overwritten).
+ *   dX        : out, bf16 [N, D] (overwritten). Until the call's last kernel writes
+ *               it, the buffer serves as scratch: the backward gathers the valid rows
+ *               of X there and runs its GEMMs on them alone (an ignored row's gradient
+ *               is zero). A dX that overlaps an input (X itself, say) is computed in
+ *               place without that compaction.
  *   dW        : out, fp32 [D, V] (overwritten, each element written once).
  *   workspace : device scratch of at least flce_workspace_size(N,D,V,1) bytes.
  * The options must equal the forward call's. FLCE_REDUCTION_NONE is refused

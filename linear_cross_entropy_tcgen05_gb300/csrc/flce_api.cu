@@ -596,10 +596,10 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const float* out_scale = pb.f16 ? gval : nullptr;  // dW, dX = g / kF16GradScale * (f16 band GEMM)
   const bool add_grads = opt && opt->accumulate_grads;  // dW (and dbias) += this call's gradient
   // Valid-row compaction: an ignored row's gradient is zero, so the GEMMs take only the
-  // valid rows (gathered into the dX buffer) -- for the whole batch at once, a 16-bit dX
-  // and no dbias (whose column sums would read the band's unused rows).
-  const bool compact = FLCE_COMPACT_ROWS && !f32_out && Nb == pb.N && !(opt && opt->dbias) &&
-                       dx_free_for_scratch(pb, opt, lse, grad_out, dX);
+  // valid rows (gathered into the dX buffer) -- for the whole batch at once and a 16-bit
+  // dX.
+  const bool compact =
+      FLCE_COMPACT_ROWS && !f32_out && Nb == pb.N && dx_free_for_scratch(pb, opt, lse, grad_out, dX);
   int* n_valid_dev = reinterpret_cast<int*>(ws + kHdrNValid);
   int* rows = reinterpret_cast<int*>(ws + L.rows);
   int* slot = reinterpret_cast<int*>(ws + L.slot);
@@ -719,6 +719,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         cp.f16 = pb.f16 ? 1 : 0;
         cp.scale = pb.f16 ? gval : nullptr;
         cp.scale_mul = 1.f / kF16GradScale;
+        cp.dyn_rows = dyn;
         FLCE_CUDA_CHECK(launch_colsum(cp, stream));
       }
 

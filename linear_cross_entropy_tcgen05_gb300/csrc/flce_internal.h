@@ -233,6 +233,7 @@ struct ColsumParams {
   int f16;               // the band holds f16 values
   const float* scale;    // null, or column sums are multiplied by *scale * scale_mul
   float scale_mul;
+  const int* dyn_rows;   // device count of the band's rows to sum (compacted valid rows), or null
 };
 
 // Rows of one GEMM output tile (a CTA pair: 2 x 128).

@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(256) flce_colsum_partial_kernel(const ColsumPa
   if (col >= p.cols) return;
   const int rows_per = (p.N + p.row_chunks - 1) / p.row_chunks;
   const int r0 = int(blockIdx.y) * rows_per;
-  const int r1 = min(p.N, r0 + rows_per);
+  // compacted rows: the band holds the valid rows first; the rest was not written
+  const int n = p.dyn_rows != nullptr ? min(p.N, *p.dyn_rows) : p.N;
+  const int r1 = min(n, r0 + rows_per);
   float s = 0.f;
   if (p.f16) {
     for (int r = r0; r < r1; ++r) s += __half2float(__ushort_as_half(p.band[size_t(r) * p.ld + col]));

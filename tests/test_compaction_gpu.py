@@ -1,9 +1,10 @@
-"""The backward's valid-row compaction: with the default options and a 16-bit dX, the
-GEMMs run on the valid rows only (gathered into the dX buffer) and dX is cast back to the
+"""The backward's valid-row compaction: with a 16-bit dX over the whole batch, the GEMMs
+run on the valid rows only (gathered into the dX buffer) and dX is cast back to the
 original rows. Results equal the uncompacted path's (taken with the fp32 dX output, which
 keeps rows in place): dX bit for bit, dW to fp32 rounding (its sum over rows runs in
 another order); the oracle checks both. Edge cases: no valid row, one valid row, a batch
-that is mostly ignored, and a dX buffer that aliases X (no scratch: no compaction)."""
+that is mostly ignored, a dX buffer that aliases X (no scratch: no compaction), and dbias
+summed over the compacted band."""
 import numpy as np
 import pytest
 import torch
@@ -21,7 +22,7 @@ def _ws(N, D, V):
     return torch.empty(flce.flce_workspace_size(N, D, V, 2), dtype=torch.uint8, device=DEV)
 
 
-def _both_paths(X, W, y, common, options_extra=None):
+def _both_paths(X, W, y, common):
     """(dX bf16, dW) compacted, and (dX fp32, dW) uncompacted, on the same inputs."""
     N, D = X.shape
     V = W.shape[1]
@@ -96,3 +97,31 @@ def test_dx_aliasing_x_is_computed_in_place(gpu_lib):
     _, _, ref_dX, ref_dW = oracle.forward_backward(X, W, y, *common)
     assert rel_fro(Xd.float().cpu().numpy(), ref_dX) <= TOL_DX_REL
     assert rel_fro(dW.cpu().numpy(), ref_dW) <= TOL_DW_REL
+
+
+def test_compacted_dbias(gpu_lib):
+    """With a bias, the dbias column sums stop at the valid-row count of the compacted band."""
+    wl = custom("compact_bias", 1300, 136, 3000, seed=85, ignore_frac=0.3, label_smoothing=0.1)
+    X, W, y = make_inputs(wl)
+    bias = torch.tensor(np.random.default_rng(86).standard_normal(wl.V) * 0.5, dtype=torch.float32)
+    N, D, V = wl.N, wl.D, wl.V
+    common = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    Xd, Wd, yd, bd = X.to(DEV), W.to(DEV), y.to(DEV), bias.to(DEV)
+    loss, lse = torch.empty(1, device=DEV), torch.empty(N, device=DEV)
+    ws = _ws(N, D, V)
+    flce.flce_forward_ex(Xd, Wd, yd, loss, lse, ws, *common, options=flce.make_options(bias=bd))
+    g = torch.ones(1, device=DEV)
+    outs = []
+    for f32 in (False, True):
+        dX = torch.empty(N, D, dtype=torch.bfloat16, device=DEV)
+        dX32 = torch.empty(N, D, device=DEV) if f32 else None
+        dW = torch.empty(D, V, device=DEV)
+        db = torch.full((V,), float("nan"), device=DEV)
+        flce.flce_backward_ex(Xd, Wd, yd, lse, g, None if f32 else dX, dW, ws, *common,
+                              options=flce.make_options(bias=bd, dbias=db, dX_f32=dX32))
+        assert flce.flce_check_device_error(ws) == 0
+        outs.append(db.cpu().numpy())
+    torch.cuda.synchronize()
+    assert rel_fro(outs[0], outs[1]) <= 1e-5
+    _, _, _, _, ref_db = oracle.forward_backward_ext(X, W, y, *common, bias=bias)
+    assert rel_fro(outs[0], ref_db) <= TOL_DW_REL

@@ -9,9 +9,9 @@
 // Backward ("Backward Pass" and "Path to Production" of the same post; PR #1291: dW
 //           contracts over the tokens and is written once):
 //   1. prep: number of valid rows, g (over the whole batch), per-row coefficients; with
-//      the default options and a 16-bit dX, the valid rows' X and coefficients are
-//      gathered to the front of the dX buffer (ignored rows have a zero gradient, so the
-//      GEMMs below skip them) and the GEMMs read the device's row count;
+//      a 16-bit dX, the valid rows' X and coefficients are gathered to the front of the
+//      (row band's) dX buffer (ignored rows have a zero gradient, so the GEMMs below skip
+//      them) and the GEMMs read the device's row count;
 //   2. for every band of Vc vocabulary columns (Vc picked so that the dW launches fill
 //      whole waves of resident clusters), and for every row band when row_band is set:
 //        gradient GEMM : recompute the logits, G = dZ in bf16 (f16: scaled) into the band;
@@ -596,10 +596,8 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const float* out_scale = pb.f16 ? gval : nullptr;  // dW, dX = g / kF16GradScale * (f16 band GEMM)
   const bool add_grads = opt && opt->accumulate_grads;  // dW (and dbias) += this call's gradient
   // Valid-row compaction: an ignored row's gradient is zero, so the GEMMs take only the
-  // valid rows (gathered into the dX buffer) -- for the whole batch at once and a 16-bit
-  // dX.
-  const bool compact =
-      FLCE_COMPACT_ROWS && !f32_out && Nb == pb.N && dx_free_for_scratch(pb, opt, lse, grad_out, dX);
+  // valid rows, gathered into the row band's part of the 16-bit dX buffer.
+  const bool compact = FLCE_COMPACT_ROWS && !f32_out && dx_free_for_scratch(pb, opt, lse, grad_out, dX);
   int* n_valid_dev = reinterpret_cast<int*>(ws + kHdrNValid);
   int* rows = reinterpret_cast<int*>(ws + L.rows);
   int* slot = reinterpret_cast<int*>(ws + L.slot);
@@ -648,9 +646,11 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
   const int64_t d_tiles_n = cdiv(pb.D, kBN);                         // dX columns
   for (int64_t n0 = 0; n0 < pb.N; n0 += Nb) {
     const int64_t nb = (pb.N - n0 < Nb) ? pb.N - n0 : Nb;
-    // the GEMMs' X: this row band of X, or its valid rows compacted into the dX buffer
-    const void* Xb = compact ? dX : static_cast<const void*>(static_cast<const uint8_t*>(pb.X) +
-                                                             size_t(n0) * size_t(pb.D) * 2);
+    // the GEMMs' X: this row band of X, or its valid rows compacted into the band's dX rows
+    const size_t band_off = size_t(n0) * size_t(pb.D) * 2;
+    const void* Xrows = static_cast<const uint8_t*>(pb.X) + band_off;
+    void* dXrows = compact ? static_cast<uint8_t*>(dX) + band_off : nullptr;
+    const void* Xb = compact ? static_cast<const void*>(dXrows) : Xrows;
     float* dx_dst = f32_out ? opt->dX_f32 + size_t(n0) * size_t(pb.D) : dx_acc;
     CUtensorMap tmXk, tmXmn, tmG, tmGmn, tmDX;
     const bool enc =
@@ -672,9 +672,9 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
     const float4* coef_rows = coef;
     const int* dyn = nullptr;
     if (compact) {
-      const CompactParams cp{pb.targets, int(pb.N), pb.ignore_index, rows, slot, n_valid_dev};
+      const CompactParams cp{pb.targets + n0, int(nb), pb.ignore_index, rows, slot, n_valid_dev};
       FLCE_CUDA_CHECK(launch_compact_rows(cp, stream));
-      const GatherParams gp{pb.X, dX, coef, coef_c, rows, n_valid_dev, int(pb.N), int(pb.D)};
+      const GatherParams gp{Xrows, dXrows, coef, coef_c, rows, n_valid_dev, int(nb), int(pb.D)};
       FLCE_CUDA_CHECK(launch_gather_rows(gp, sms, stream));
       coef_rows = coef_c;
       dyn = n_valid_dev;
@@ -762,7 +762,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, pb.f16, stream));
     }
     if (compact) {
-      const ScatterCastParams sc{dx_acc, dX, slot, int(pb.N), int(pb.D), pb.f16 ? 1 : 0};
+      const ScatterCastParams sc{dx_acc, dXrows, slot, int(nb), int(pb.D), pb.f16 ? 1 : 0};
       FLCE_CUDA_CHECK(launch_scatter_cast(sc, sms, stream));
     } else if (!f32_out) {
       void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;

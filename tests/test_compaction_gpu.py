@@ -1,10 +1,10 @@
-"""The backward's valid-row compaction: with a 16-bit dX over the whole batch, the GEMMs
-run on the valid rows only (gathered into the dX buffer) and dX is cast back to the
-original rows. Results equal the uncompacted path's (taken with the fp32 dX output, which
+"""The backward's valid-row compaction: with a 16-bit dX, the GEMMs run on the valid rows
+only (gathered into the dX buffer, per row band when there are row bands) and dX is cast
+back to the original rows. Results equal the uncompacted path's (taken with the fp32 dX output, which
 keeps rows in place): dX bit for bit, dW to fp32 rounding (its sum over rows runs in
 another order); the oracle checks both. Edge cases: no valid row, one valid row, a batch
 that is mostly ignored, a dX buffer that aliases X (no scratch: no compaction), and dbias
-summed over the compacted band."""
+summed over the compacted band; row bands."""
 import numpy as np
 import pytest
 import torch
@@ -22,7 +22,7 @@ def _ws(N, D, V):
     return torch.empty(flce.flce_workspace_size(N, D, V, 2), dtype=torch.uint8, device=DEV)
 
 
-def _both_paths(X, W, y, common):
+def _both_paths(X, W, y, common, row_band=0):
     """(dX bf16, dW) compacted, and (dX fp32, dW) uncompacted, on the same inputs."""
     N, D = X.shape
     V = W.shape[1]
@@ -33,11 +33,12 @@ def _both_paths(X, W, y, common):
     g = torch.ones(1, device=DEV)
     dX = torch.full((N, D), float("nan"), dtype=torch.bfloat16, device=DEV)
     dW = torch.full((D, V), float("nan"), device=DEV)
-    flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *common)
+    flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, ws, *common, options=flce.make_options(row_band=row_band))
     assert flce.flce_check_device_error(ws) == 0
     dX32 = torch.full((N, D), float("nan"), device=DEV)
     dW2 = torch.full((D, V), float("nan"), device=DEV)
-    flce.flce_backward_ex(Xd, Wd, yd, lse, g, None, dW2, ws, *common, options=flce.make_options(dX_f32=dX32))
+    flce.flce_backward_ex(Xd, Wd, yd, lse, g, None, dW2, ws, *common,
+                          options=flce.make_options(dX_f32=dX32, row_band=row_band))
     assert flce.flce_check_device_error(ws) == 0
     torch.cuda.synchronize()
     return dX.cpu(), dW.cpu().numpy(), dX32.cpu(), dW2.cpu().numpy()
@@ -125,3 +126,18 @@ def test_compacted_dbias(gpu_lib):
     assert rel_fro(outs[0], outs[1]) <= 1e-5
     _, _, _, _, ref_db = oracle.forward_backward_ext(X, W, y, *common, bias=bias)
     assert rel_fro(outs[0], ref_db) <= TOL_DW_REL
+
+
+@pytest.mark.parametrize("row_band", [384, 1000])
+def test_compaction_per_row_band(gpu_lib, row_band):
+    """Row bands: each band's valid rows are compacted into that band's rows of dX."""
+    wl = custom("compact_band", 2500, 136, 3000, seed=87, ignore_frac=0.3, label_smoothing=0.1, zloss_scale=1e-3)
+    X, W, y = make_inputs(wl)
+    y[:400] = IGNORE_INDEX  # a whole band (or most of one) without a valid row
+    common = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    dX, dW, dX32, dW2 = _both_paths(X, W, y, common, row_band)
+    assert torch.equal(dX, dX32.to(torch.bfloat16))
+    assert rel_fro(dW, dW2) <= 1e-5
+    _, _, ref_dX, ref_dW = oracle.forward_backward(X, W, y, *common)
+    assert rel_fro(dX.float().numpy(), ref_dX) <= TOL_DX_REL
+    assert rel_fro(dW, ref_dW) <= TOL_DW_REL

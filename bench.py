@@ -148,20 +148,21 @@ def barrier(world: int):
         dist.barrier()
 
 
-def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True):
+def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band=0):
     """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
-    backward denominator + row coefficients (+ valid-row compaction and gather) + 3 GEMMs
-    per vocabulary band + the dX cast. vc is the band width (flce_backward_band_width on
-    the device); without it, the workspace's band capacity. compact: the backward
-    compacts the valid rows (the default options with a 16-bit dX)."""
+    backward denominator, then per row band (one, or ceil(N / row_band)) row coefficients
+    (+ valid-row compaction and gather) + 3 GEMMs per vocabulary band + the dX cast. vc is
+    the band width (flce_backward_band_width on the device); without it, the workspace's
+    band capacity. compact: the backward compacts the valid rows (a 16-bit dX)."""
+    rows = row_band if 0 < row_band < N else N
     if vc is None:
         unit = 512  # one cluster's vocabulary tiles: 2 CTA pairs x 256
-        vc = max(unit, min(16384, ((3 << 28) // (2 * N)) // unit * unit))
+        vc = max(unit, min(16384, ((3 << 28) // (2 * rows)) // unit * unit))
         half = (((V + 1) // 2) + unit - 1) // unit * unit
         vc = min(vc, half)
     bands = -(-V // vc)
     fwd = 1 + 1 + (0 if reduction == "none" else 1)
-    bwd = 2 + (2 if compact else 0) + 3 * bands + 1
+    bwd = 1 + -(-N // rows) * (1 + (2 if compact else 0) + 3 * bands + 1)
     return fwd + bwd, bands, vc
 
 
@@ -255,7 +256,10 @@ def run_ours(args, wl, world, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     ws_f = flce.flce_workspace_size(N, D, V, False)
-    ws_b = flce.flce_workspace_size(N, D, V, True)
+    # memory-lean backward (row bands): a workspace for row_band rows whatever N is
+    row_band = args.row_band if 0 < args.row_band < N else 0
+    opt_b = flce.make_options(row_band=row_band) if row_band else None
+    ws_b = flce.flce_workspace_size(row_band or N, D, V, True)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     g = torch.ones(1, dtype=torch.float32, device=dev)
@@ -272,7 +276,10 @@ def run_ours(args, wl, world, rank, local):
         flce.flce_forward(Xd, Wd, yd, loss, lse, ws, *opts, stream=stream)
 
     def bwd():
-        flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, stream=stream)
+        if opt_b is None:
+            flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, stream=stream)
+        else:
+            flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, options=opt_b, stream=stream)
 
     if args.only is not None:
         # profiling driver: warm-up + steps of one phase, nothing else on the device
@@ -344,7 +351,7 @@ def run_ours(args, wl, world, rank, local):
     e2e_value, e2e_ms, h2d, d2h = run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd)
     return finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc,
                   extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed,
-                  flce.flce_backward_band_width(N, D, V) or None)
+                  flce.flce_backward_band_width(N, D, V, opt_b) or None)
 
 
 def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
@@ -402,7 +409,11 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
         stream.wait_event(inputs_ready[b])
         stream.wait_event(outputs_free[b])
         flce.flce_forward(Xb, Wb, yb, lb, lse, ws_e2e, *opts, stream=stream)
-        flce.flce_backward(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts, stream=stream)
+        if args.row_band and 0 < args.row_band < N:
+            flce.flce_backward_ex(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts,
+                                  options=flce.make_options(row_band=args.row_band), stream=stream)
+        else:
+            flce.flce_backward(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts, stream=stream)
         inputs_free[b].record(stream)
         outputs_ready[b].record(stream)
         with torch.cuda.stream(s_out):
@@ -430,7 +441,8 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
     bwd_tf = 6.0 * N * D * V / (statistics.mean(bwd_ms) / 1000.0) / 1e12
     burst = float(peaks["bf16_tflops"])
     sustained = float(peaks.get("bf16_tflops_sustained", burst))
-    launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width)
+    launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width,
+                                                   row_band=args.row_band if 0 < args.row_band < N else 0)
 
     if rank != 0:
         return
@@ -454,7 +466,8 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
         "config": {"workload": wl.name, "N": N, "D": D, "V": V, "reduction": wl.reduction,
                    "ignore_frac": wl.ignore_frac, "grad_out": 1.0,
                    "l2": "inputs larger than L2 (X 0.54 GB, W 1.05 GB > 129 MB); no flush",
-                   "parallelism": f"replicas x{world}", "vocab_band": vc, "bands": bands},
+                   "parallelism": f"replicas x{world}", "vocab_band": vc, "bands": bands,
+                   **({"row_band": args.row_band} if 0 < args.row_band < N else {})},
         "pct_bf16_peak": 100.0 * step_tf / burst,
         "tflops": step_tf,
         "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms),
@@ -510,6 +523,8 @@ def main():
     ap.add_argument("--oracle-rows", type=int, default=512, help="rows per step of the reference arm")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU time of the cpu_baseline sample")
     ap.add_argument("--shape", default=None, help="N,D,V override of the workload's shape (profiling cases)")
+    ap.add_argument("--row-band", type=int, default=0,
+                    help="memory-lean backward: rows per band (0: the whole batch at once)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--wait-stats", action="store_true",

@@ -51,6 +51,8 @@ def test_launch_count_matches_the_band_schedule():
     assert bands == 28 and total == 3 + 4 + 3 * 28 + 1                  # a narrower band chosen on the device
     total, _, _ = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608, compact=False)
     assert total == 3 + 2 + 3 * 28 + 1                                  # no valid-row compaction
+    total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", row_band=16384)
+    assert (bands, vc) == (8, 16384) and total == 3 + 1 + 4 * (1 + 2 + 3 * 8 + 1)   # four row bands
 
 
 def test_clock_record_decides_a_remeasurement():

@@ -6,13 +6,17 @@ ignored rows, mean reduction -- the Llama-3-8B language-model head of "Cutting L
 Memory by 84%: A Deep Dive into Fused Kernels" ("The Logit Bottleneck") and of the
 Liger-Kernel PR #1291 BT sweep. Inputs are synthetic (seeded, see workloads).
 
-Prints ONE JSON line (rank 0). Launch with torchrun for several GPUs: each rank runs
-its own replica of the workload (weak scaling, no collective on the data path).
+Prints ONE JSON line. The GPU arm runs on one GPU in one process: its GEMMs share
+operand tiles between the CTAs of a cluster with TMA multicast, which this library
+keeps to single-GPU processes, so a launch with WORLD_SIZE > 1 or --gpus > 1 is
+refused before the library is loaded. Beside the headline figure the line carries the
+other four workloads and the memory-benchmark shape ("workloads"), each timed for a
+fraction of a second.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the fp64 CPU oracle on bounded samples of the same workload
-(the reference arm); it runs on rank 0 only.
+(the reference arm); under torchrun only rank 0 runs it, the other ranks exit 0.
 """
 from __future__ import annotations
 
@@ -119,33 +123,25 @@ class ClockSampler:
         return out
 
 
-def dist_setup(n_gpus: int):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    return world, rank, local
+def launch_env():
+    """(world size, rank) of a torchrun launch, or (1, 0) for a plain process. No process
+    group is ever created: the GPU arm refuses a world size above one, and the reference
+    arm runs on rank 0 alone."""
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
-def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else torch.device("cpu")
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+ONE_GPU_ONLY = ("one GPU per process only: the GEMMs share each operand tile among the CTAs of a "
+                "cluster with TMA multicast, which this library keeps to single-GPU processes; "
+                "run bench.py without torchrun and with --gpus 1")
 
 
-def barrier(world: int):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+def refuse_multi_gpu(args, world: int, rank: int) -> int:
+    """The GPU arm in a launch of several processes or GPUs: print why (rank 0) and return
+    the exit status, before the library is loaded or a device is touched."""
+    if rank == 0:
+        print(json.dumps({"impl": "ours", "n_gpus": max(args.gpus, world), "unavailable": ONE_GPU_ONLY}), flush=True)
+    print(f"bench.py: {ONE_GPU_ONLY}", file=sys.stderr, flush=True)
+    return 2
 
 
 def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band=0):
@@ -215,11 +211,9 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
-def run_reference(args, wl, world, rank):
-    if rank != 0:
-        return
+def run_reference(args, wl):
     X, W, y = make_inputs(wl)
-    rows = args.oracle_rows
+    rows = min(args.oracle_rows, wl.N)
     rates, times = [], []
     for _ in range(args.warmup):
         oracle_sample_rate(wl, X, W, y, rows)
@@ -227,16 +221,17 @@ def run_reference(args, wl, world, rank):
         r, dt = oracle_sample_rate(wl, X, W, y, rows)
         rates.append(r)
         times.append(dt)
-    value = statistics.median(rates)
+    ms_step = 1000.0 * statistics.median(times)
+    value = rows / (ms_step / 1000.0)
     sample = (f"fp64 oracle fwd+bwd of {rows} rows x full V={wl.V} (D={wl.D}) per step; "
               f"tokens/s = rows / time; {args.steps} steps after {args.warmup} warm-up")
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * wl.N / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D), uniform targets, 5% ignored)",
         "config": {"workload": wl.name, "N": wl.N, "D": wl.D, "V": wl.V, "reduction": wl.reduction,
-                   "ignore_frac": wl.ignore_frac},
+                   "ignore_frac": wl.ignore_frac, "rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -245,54 +240,102 @@ def run_reference(args, wl, world, rank):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_ours(args, wl, world, rank, local):
+class Problem:
+    """Device buffers of one workload and its forward / backward calls on one stream."""
+
+    def __init__(self, flce, wl, dev, stream, X, W, y, row_band=0):
+        self.flce, self.wl, self.dev, self.stream = flce, wl, dev, stream
+        N, D, V = wl.N, wl.D, wl.V
+        self.X, self.W, self.y = X, W, y
+        self.ws_f = flce.flce_workspace_size(N, D, V, False)
+        self.row_band = row_band if 0 < row_band < N else 0
+        self.opt_b = flce.make_options(row_band=self.row_band) if self.row_band else None
+        self.ws_b = flce.flce_workspace_size(self.row_band or N, D, V, True)
+        self.loss = torch.empty(1, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(N, dtype=torch.float32, device=dev)
+        self.g = torch.ones(1, dtype=torch.float32, device=dev)
+        self.dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev)
+        self.dW = torch.empty(D, V, dtype=torch.float32, device=dev)
+        self.opts = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+        self.ws = None
+
+    def io_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.X, self.W, self.y, self.loss, self.lse, self.dX,
+                                                           self.dW))
+
+    def alloc_workspace(self, with_bwd=True):
+        self.ws = torch.empty(max(self.ws_f, self.ws_b) if with_bwd else self.ws_f, dtype=torch.uint8,
+                              device=self.dev)
+
+    def fwd(self):
+        self.flce.flce_forward(self.X, self.W, self.y, self.loss, self.lse, self.ws, *self.opts, stream=self.stream)
+
+    def bwd(self):
+        if self.opt_b is None:
+            self.flce.flce_backward(self.X, self.W, self.y, self.lse, self.g, self.dX, self.dW, self.ws, *self.opts,
+                                    stream=self.stream)
+        else:
+            self.flce.flce_backward_ex(self.X, self.W, self.y, self.lse, self.g, self.dX, self.dW, self.ws,
+                                       *self.opts, options=self.opt_b, stream=self.stream)
+
+    def check(self, where):
+        st = self.flce.flce_check_device_error(self.ws, self.stream)
+        if st != 0:
+            raise RuntimeError(f"device error {where}: {self.flce.flce_status_string(st)}")
+
+    def timed_steps(self, steps, gpu_index):
+        """`steps` forward + backward steps on the stream, each bracketed by CUDA events;
+        returns (total ms, per-step forward ms, per-step backward ms, launches, clocks)."""
+        flce = self.flce
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize(self.dev)
+        launches_before = flce.flce_kernel_launches()
+        with ClockSampler(gpu_index) as clk:
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(self.stream)
+            for i in range(steps):
+                ev[i][0].record(self.stream)
+                self.fwd()
+                ev[i][1].record(self.stream)
+                self.bwd()
+                ev[i][2].record(self.stream)
+            end.record(self.stream)
+            launches = flce.flce_kernel_launches() - launches_before
+            torch.cuda.synchronize(self.dev)
+        self.check("in the timed region")
+        return (start.elapsed_time(end), [a.elapsed_time(b) for a, b, _ in ev],
+                [b.elapsed_time(c) for _, b, c in ev], launches, clk)
+
+
+def run_ours(args, wl):
     import linear_cross_entropy_tcgen05_gb300 as flce
     flce.load_library()
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     N, D, V = wl.N, wl.D, wl.V
-    X, W, y = make_inputs(wl, seed=wl.seed + 1000 * rank)
-    Xd, Wd, yd = X.to(dev), W.to(dev), y.to(dev)
+    X, W, y = make_inputs(wl)
     stream = torch.cuda.current_stream(dev)
-
-    ws_f = flce.flce_workspace_size(N, D, V, False)
-    # memory-lean backward (row bands): a workspace for row_band rows whatever N is
-    row_band = args.row_band if 0 < args.row_band < N else 0
-    opt_b = flce.make_options(row_band=row_band) if row_band else None
-    ws_b = flce.flce_workspace_size(row_band or N, D, V, True)
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
-    lse = torch.empty(N, dtype=torch.float32, device=dev)
-    g = torch.ones(1, dtype=torch.float32, device=dev)
+    pb = Problem(flce, wl, dev, stream, X.to(dev), W.to(dev), y.to(dev), row_band=args.row_band)
     with_bwd = args.only != "fwd"
-    dX = torch.empty(N, D, dtype=torch.bfloat16, device=dev) if with_bwd else None
-    dW = torch.empty(D, V, dtype=torch.float32, device=dev) if with_bwd else None
     torch.cuda.synchronize(dev)
     base_alloc = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    ws = torch.empty(max(ws_f, ws_b) if with_bwd else ws_f, dtype=torch.uint8, device=dev)
-    opts = (wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
-
-    def fwd():
-        flce.flce_forward(Xd, Wd, yd, loss, lse, ws, *opts, stream=stream)
-
-    def bwd():
-        if opt_b is None:
-            flce.flce_backward(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, stream=stream)
-        else:
-            flce.flce_backward_ex(Xd, Wd, yd, lse, g, dX, dW, ws, *opts, options=opt_b, stream=stream)
+    pb.alloc_workspace(with_bwd)
 
     if args.only is not None:
         # profiling driver: warm-up + steps of one phase, nothing else on the device
         if args.only == "bwd":
-            fwd()
-        step = fwd if args.only == "fwd" else bwd
+            pb.fwd()
+        step = pb.fwd if args.only == "fwd" else pb.bwd
         for _ in range(args.warmup + args.steps):
             step()
         torch.cuda.synchronize(dev)
         line = {"only": args.only, "workload": wl.name}
         if args.wait_stats:
-            line["pipeline_waits"] = pipeline_waits(ws, args.only)
-        st = flce.flce_check_device_error(ws, stream)
+            line["pipeline_waits"] = pipeline_waits(pb.ws, args.only)
+        st = flce.flce_check_device_error(pb.ws, stream)
         line["status"] = flce.flce_status_string(st)
         print(json.dumps(line))
         if st != 0:
@@ -300,61 +343,36 @@ def run_ours(args, wl, world, rank, local):
         return
 
     for _ in range(args.warmup):
-        fwd()
-        bwd()
+        pb.fwd()
+        pb.bwd()
     torch.cuda.synchronize(dev)
-    st = flce.flce_check_device_error(ws, stream)
-    if st != 0:
-        raise RuntimeError(f"device error after warm-up: {flce.flce_status_string(st)}")
+    pb.check("after warm-up")
     peak_alloc = torch.cuda.max_memory_allocated(dev)
     extra_bytes = peak_alloc - base_alloc
 
-    def timed_region():
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        launches_before = flce.flce_kernel_launches()
-        with ClockSampler(local) as clk:
-            start = torch.cuda.Event(enable_timing=True)
-            end = torch.cuda.Event(enable_timing=True)
-            start.record(stream)
-            for i in range(args.steps):
-                ev[i][0].record(stream)
-                fwd()
-                ev[i][1].record(stream)
-                bwd()
-                ev[i][2].record(stream)
-            end.record(stream)
-            launches = flce.flce_kernel_launches() - launches_before
-            torch.cuda.synchronize(dev)
-            barrier(world)
-        st = flce.flce_check_device_error(ws, stream)
-        if st != 0:
-            raise RuntimeError(f"device error in the timed region: {flce.flce_status_string(st)}")
-        return (start.elapsed_time(end), [a.elapsed_time(b) for a, b, _ in ev],
-                [b.elapsed_time(c) for _, b, c in ev], launches, clk)
-
-    total_ms, fwd_ms, bwd_ms, launches_timed, clk = timed_region()
+    total_ms, fwd_ms, bwd_ms, launches_timed, clk = pb.timed_steps(args.steps, 0)
     # a run that saw thermal or hardware slowdown, or clocks held far below maximum with no
-    # reason given (a leftover clock lock), is measured once more (the decision is taken
-    # over all ranks so that they stay in step)
-    bad = float(clk.throttled())
-    if max_over_ranks(bad, world) > 0:
-        total_ms, fwd_ms, bwd_ms, launches_timed, clk = timed_region()
+    # reason given (a leftover clock lock), is measured once more
+    if clk.throttled():
+        total_ms, fwd_ms, bwd_ms, launches_timed, clk = pb.timed_steps(args.steps, 0)
         clk.remeasured = True
-    total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
-    value = world * N / (ms_step / 1000.0)
+    value = N / (ms_step / 1000.0)
+    band_width = flce.flce_backward_band_width(N, D, V, pb.opt_b) or None
 
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
-    e2e_value, e2e_ms, h2d, d2h = run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd)
-    return finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc,
-                  extra_bytes, ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed,
-                  flce.flce_backward_band_width(N, D, V, opt_b) or None)
+    e2e_value, e2e_ms, h2d, d2h = run_e2e(args, dev, stream, X, W, y, pb)
+    del pb
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    side = run_side_workloads(args, flce, dev, stream) if args.side_workloads else None
+    return finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
+                  e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width, side,
+                  flce.flce_workspace_size(N, D, V, False),
+                  flce.flce_workspace_size(args.row_band if 0 < args.row_band < N else N, D, V, True))
 
 
-def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bwd):
+def run_e2e(args, dev, stream, X, W, y, pb):
     """End to end through the public API: every step copies X, W and targets from pinned
     host memory to the device and loss, dX and dW back. Copies run on their own streams
     with three buffer sets, so step i's compute overlaps the input copy of step i+1 and the
@@ -362,7 +380,7 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
     slack before compute waits for it (what a training loop feeding this op would do)."""
     if args.no_e2e:
         return None, None, 0, 0
-    import linear_cross_entropy_tcgen05_gb300 as flce
+    flce = pb.flce
     N, D = X.shape
     V = W.shape[1]
     Xh, Wh, yh = X.pin_memory(), W.pin_memory(), y.pin_memory()
@@ -373,20 +391,16 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
     d2h = 4 + dX_h.numel() * 2 + dW_h.numel() * 4
     # buffer sets: set 0 reuses the resident buffers, the others are copies
     nbuf = 3
-    bufs = [(Xd, Wd, yd, loss, dX, dW)] + [
-        (torch.empty_like(Xd), torch.empty_like(Wd), torch.empty_like(yd), torch.empty_like(loss),
-         torch.empty_like(dX), torch.empty_like(dW)) for _ in range(nbuf - 1)]
-    nbytes = max(flce.flce_workspace_size(N, D, V, 0), flce.flce_workspace_size(N, D, V, 1))
-    ws_e2e = torch.empty(nbytes, dtype=torch.uint8, device=dev)  # compute is serialised on one stream
+    bufs = [(pb.X, pb.W, pb.y, pb.loss, pb.dX, pb.dW)] + [
+        (torch.empty_like(pb.X), torch.empty_like(pb.W), torch.empty_like(pb.y), torch.empty_like(pb.loss),
+         torch.empty_like(pb.dX), torch.empty_like(pb.dW)) for _ in range(nbuf - 1)]
     lse = torch.empty(N, dtype=torch.float32, device=dev)
-    g = torch.ones(1, dtype=torch.float32, device=dev)
     s_in = torch.cuda.Stream(dev)
     s_out = torch.cuda.Stream(dev)
     inputs_free = [torch.cuda.Event() for _ in range(nbuf)]
     inputs_ready = [torch.cuda.Event() for _ in range(nbuf)]
     outputs_ready = [torch.cuda.Event() for _ in range(nbuf)]
     outputs_free = [torch.cuda.Event() for _ in range(nbuf)]
-    opts = (args._wl.ignore_index, args._wl.label_smoothing, args._wl.zloss_scale, args._wl.reduction)
     steps = max(1, args.steps)
     warm = nbuf
     for ev in inputs_free + outputs_free:
@@ -396,7 +410,6 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
     for it in range(warm + steps):
         if it == warm:
             torch.cuda.synchronize(dev)
-            barrier(world)
             t0.record(stream)
         b = it % nbuf
         Xb, Wb, yb, lb, dXb, dWb = bufs[b]
@@ -408,12 +421,13 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
             inputs_ready[b].record(s_in)
         stream.wait_event(inputs_ready[b])
         stream.wait_event(outputs_free[b])
-        flce.flce_forward(Xb, Wb, yb, lb, lse, ws_e2e, *opts, stream=stream)
-        if args.row_band and 0 < args.row_band < N:
-            flce.flce_backward_ex(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts,
-                                  options=flce.make_options(row_band=args.row_band), stream=stream)
+        # compute is serialised on one stream, so every buffer set shares the workspace
+        flce.flce_forward(Xb, Wb, yb, lb, lse, pb.ws, *pb.opts, stream=stream)
+        if pb.opt_b is not None:
+            flce.flce_backward_ex(Xb, Wb, yb, lse, pb.g, dXb, dWb, pb.ws, *pb.opts, options=pb.opt_b,
+                                  stream=stream)
         else:
-            flce.flce_backward(Xb, Wb, yb, lse, g, dXb, dWb, ws_e2e, *opts, stream=stream)
+            flce.flce_backward(Xb, Wb, yb, lse, pb.g, dXb, dWb, pb.ws, *pb.opts, stream=stream)
         inputs_free[b].record(stream)
         outputs_ready[b].record(stream)
         with torch.cuda.stream(s_out):
@@ -425,14 +439,88 @@ def run_e2e(args, world, dev, stream, X, W, y, Xd, Wd, yd, loss, dX, dW, fwd, bw
     stream.wait_stream(s_out)
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(t0.elapsed_time(t1) / steps, world)
-    e2e_value = world * N / (e2e_ms / 1000.0)
+    pb.check("in the end-to-end region")
+    e2e_ms = t0.elapsed_time(t1) / steps
+    e2e_value = N / (e2e_ms / 1000.0)
     del bufs
     return e2e_value, e2e_ms, h2d, d2h
 
 
-def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
-           ws_f, ws_b, e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width):
+def device_inputs(wl, dev):
+    """Inputs of a side workload drawn on the device: X ~ N(0,1) and W ~ N(0,1/D) from
+    torch's seeded device generator, rounded to bf16 (the recipe's distributions, drawn in
+    a fraction of a second where the host recipe takes seconds per gigabyte), and the
+    recipe's own targets and ignored rows."""
+    from workloads import make_targets_of
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.seed)
+    X = torch.randn(wl.N, wl.D, generator=gen, device=dev).to(torch.bfloat16)
+    W = torch.randn(wl.D, wl.V, generator=gen, device=dev).mul_(1.0 / math.sqrt(wl.D)).to(torch.bfloat16)
+    y = make_targets_of(wl).to(dev)
+    return X, W, y
+
+
+def run_side_workloads(args, flce, dev, stream):
+    """The other workloads and the memory-benchmark shape, each warmed up and then timed
+    for about `args.side_seconds` (at least 5 steps): median fwd+bwd step, tokens/s, the
+    fraction of the sustained bf16 peak for 8*N*D*V flops, and peak device memory (total
+    for inputs, outputs and workspace; extra = beyond the inputs and outputs)."""
+    from workloads import MEMORY_BENCHMARK
+    peaks, peak_kind = measured_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    out = {}
+    chosen = [w for w in args.side_workloads.split(",") if w and w != args.workload]
+    for name in chosen:
+        wl = MEMORY_BENCHMARK if name == MEMORY_BENCHMARK.name else WORKLOADS[name]
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        X, W, y = device_inputs(wl, dev)
+        pb = Problem(flce, wl, dev, stream, X, W, y)
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        io = torch.cuda.memory_allocated(dev)
+        pb.alloc_workspace(True)
+        for _ in range(3):
+            pb.fwd()
+            pb.bwd()
+        torch.cuda.synchronize(dev)
+        pb.check(f"after the warm-up of {name}")
+        peak = torch.cuda.max_memory_allocated(dev)
+        # a short probe sets the step count for about side_seconds of timed work
+        t_probe, _, _, _, _ = pb.timed_steps(2, 0)
+        steps = int(min(400, max(5, math.ceil(args.side_seconds * 1000.0 / max(t_probe / 2, 1e-3)))))
+        total, f_ms, b_ms, launches, clk = pb.timed_steps(steps, 0)
+        step_ms = [f + b for f, b in zip(f_ms, b_ms)]
+        med = statistics.median(step_ms)
+        N, D, V = wl.N, wl.D, wl.V
+        tf = 8.0 * N * D * V / (med / 1000.0) / 1e12
+        out[name] = {
+            "N": N, "D": D, "V": V, "options": wl.describe(), "steps": steps,
+            "ms_per_step_median": med, "fwd_ms_median": statistics.median(f_ms),
+            "bwd_ms_median": statistics.median(b_ms), "ms_per_step_mean": total / steps,
+            "tokens_per_s": N / (med / 1000.0), "tflops": tf,
+            "frac_of_sustained_bf16": tf / sustained,
+            "peak_kind": f"{peak_kind} sustained cuBLAS bf16 ({sustained} TF/s)",
+            "peak_mb": {"total": (peak - base) / 2**20, "extra": (peak - io) / 2**20,
+                        "workspace": pb.ws.numel() / 2**20, "logits_bf16_would_be": N * V * 2 / 2**20},
+            "launches_per_step": launches / steps,
+            "clocks": clk.summary(),
+        }
+        if name == "llama8k":
+            out[name]["context"] = ("Liger-Kernel PR #1291, Benchmarks: CuTe-DSL FLCE fwd+bwd 25.7 ms at BT=8192, "
+                                    "V=128256, H=4096, bf16, on B200 (another system and GPU)")
+        if name == MEMORY_BENCHMARK.name:
+            out[name]["context"] = ("Cutting LLM Memory by 84%, Memory Benchmark: peak 36.02 GB eager PyTorch, "
+                                    "5.04 GB Triton FLCE, at S=16384, D=4096, V=128256 on A100 (another system)")
+        del pb, X, W, y
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return {"inputs": "X, W drawn on the device (torch's seeded generator, the recipe's distributions); "
+                      "targets and ignored rows from the recipe", "results": out}
+
+
+def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes, e2e_value, e2e_ms,
+           h2d, d2h, clk, launches_timed, band_width, side, ws_f, ws_b):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -443,31 +531,36 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
     sustained = float(peaks.get("bf16_tflops_sustained", burst))
     launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width,
                                                    row_band=args.row_band if 0 < args.row_band < N else 0)
-
-    if rank != 0:
-        return
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         rate, rows, dt = oracle_sample_for(wl, X, W, y, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"fp64 oracle fwd+bwd of the first {rows} rows x full V in chunks of 256 "
                          f"({dt:.1f} s); tokens/s = rows/time"}
-    traffic = None
+    traffic, traffic_source = None, None
     tr_path = os.path.join(ROOT, "profiles", "forward_gemm_traffic.json")
     if os.path.exists(tr_path):
         tr = json.load(open(tr_path))
         if tr.get("kernel_source_hash") == _kernel_hash():
             traffic = tr.get("bytes_per_launch")
+            traffic_source = {"kind": "recorded ncu capture of this kernel source, not measured in this run",
+                              "captured": tr.get("captured"), "case": tr.get("captured_case"),
+                              "record": "profiles/forward_gemm_traffic.json"}
+    liger_b200 = 65536 / 0.194
     out = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / PAGES_TOKENS_PER_S, "dtype": "bf16",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D) in bf16, uniform targets, 5% ignore_index)",
         "config": {"workload": wl.name, "N": N, "D": D, "V": V, "reduction": wl.reduction,
                    "ignore_frac": wl.ignore_frac, "grad_out": 1.0,
                    "l2": "inputs larger than L2 (X 0.54 GB, W 1.05 GB > 129 MB); no flush",
-                   "parallelism": f"replicas x{world}", "vocab_band": vc, "bands": bands,
+                   "parallelism": "one GPU", "vocab_band": vc, "bands": bands,
                    **({"row_band": args.row_band} if 0 < args.row_band < N else {})},
+        # another system on another GPU: context, not a baseline
+        "context": {"liger_cutedsl_flce_b200": {
+            "tokens_per_s": liger_b200, "ratio": value / liger_b200,
+            "source": "Liger-Kernel PR #1291, Benchmarks: 194 ms fwd+bwd at BT=65536, V=128256, H=4096, bf16, B200"}},
         "pct_bf16_peak": 100.0 * step_tf / burst,
         "tflops": step_tf,
         "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms),
@@ -478,6 +571,7 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
         # so its peak is the sustained cuBLAS figure; the burst fraction is given beside it
         "roofline": {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
                      "peak": sustained, "unit": "TFLOP/s", "frac": fwd_gemm_tf / sustained, "traffic": traffic,
+                     "traffic_source": traffic_source,
                      "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (kernel timed inside the step loop)",
                      "frac_of_burst": fwd_gemm_tf / burst,
                      "algorithmic": "2*N*D*V flops per launch (forward call = GEMM + finalize)"},
@@ -494,6 +588,8 @@ def finish(args, wl, world, rank, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_
         "gpu_launches_per_step_expected": launches,
         "clocks": clk.summary(),
     }
+    if side is not None:
+        out["workloads"] = side
     print(json.dumps(out), flush=True)
 
 
@@ -513,6 +609,9 @@ def _kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+SIDE_DEFAULT = "tiny,small_vocab,llama8k,large_vocab,memory_benchmark"
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -527,29 +626,29 @@ def main():
                     help="memory-lean backward: rows per band (0: the whole batch at once)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--side-workloads", default=SIDE_DEFAULT,
+                    help="comma-separated workloads timed after the main one ('' for none)")
+    ap.add_argument("--side-seconds", type=float, default=0.5, help="timed seconds per side workload")
     ap.add_argument("--wait-stats", action="store_true",
                     help="with --only and a library built with -DFLCE_WAIT_STATS=1: print pipeline wait shares")
     ap.add_argument("--only", choices=["fwd", "bwd"], default=None,
                     help="profiling driver: run only this phase (warm-up + steps), print a status line")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
-    args._wl = wl
     if args.shape:
         import dataclasses
         n, d, v = (int(x) for x in args.shape.split(","))
         wl = dataclasses.replace(wl, name=f"{wl.name}@{n}x{d}x{v}", N=n, D=d, V=v)
-        args._wl = wl
-    world, rank, local = dist_setup(args.gpus)
-    try:
-        if args.impl == "reference":
-            run_reference(args, wl, world, rank)
-        else:
-            run_ours(args, wl, world, rank, local)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    world, rank = launch_env()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return 0
+    if world > 1 or args.gpus > 1:
+        return refuse_multi_gpu(args, world, rank)
+    run_ours(args, wl)
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -1,7 +1,8 @@
 """bench.py on the GPU prints one JSON line with every key of the benchmark contract: the
 metric, the device-timed value, the roofline object of the dominant kernel, the CPU-oracle
 baseline, the end-to-end figure with its host-device bytes, the launch count and the clock
-record (the tiny workload, so that it runs in seconds)."""
+record, and the side workloads' figures (the tiny workload with one small side workload,
+so that it runs in seconds)."""
 import json
 import os
 import subprocess
@@ -15,7 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_bench_line_carries_the_contract(gpu_lib):
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny", "--steps", "3",
-                        "--warmup", "3", "--cpu-seconds", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+                        "--warmup", "3", "--cpu-seconds", "1", "--side-workloads", "small_vocab",
+                        "--side-seconds", "0.2"], capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -33,3 +35,9 @@ def test_bench_line_carries_the_contract(gpu_lib):
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 3 * d["gpu_launches_per_step_expected"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # one GPU; a figure of another system is context, not a baseline
+    assert d["n_gpus"] == 1 and d["vs_baseline"] is None and "liger_cutedsl_flce_b200" in d["context"]
+    side = d["workloads"]["results"]["small_vocab"]
+    assert side["N"] == 4096 and side["D"] == 2048 and side["V"] == 32000 and side["steps"] >= 5
+    assert side["tokens_per_s"] > 0 and abs(side["tokens_per_s"] * side["ms_per_step_median"] / 1000 - 4096) < 1e-3
+    assert side["peak_mb"]["extra"] > 0 and side["peak_mb"]["extra"] < side["peak_mb"]["logits_bf16_would_be"] / 8

@@ -1,46 +1,54 @@
-"""The benchmark's multi-rank plumbing on CPU: two gloo ranks agree on the maximum
-elapsed time and pass the barrier (each rank runs its own replica; there is no
-collective on the data path)."""
+"""The benchmark's process logic on CPU. The GPU arm is single-GPU by design (its GEMMs
+share operand tiles inside a cluster with TMA multicast, kept to one-GPU processes): a
+launch of several processes or GPUs is refused before the library is loaded. The
+reference arm (the CPU oracle) runs on rank 0 only; other ranks exit 0 without work."""
+import json
 import os
-import socket
+import subprocess
+import sys
 
 import pytest
-import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _free_port() -> int:
-    s = socket.socket()
-    s.bind(("127.0.0.1", 0))
-    port = s.getsockname()[1]
-    s.close()
-    return port
+def _bench(args, **env):
+    e = dict(os.environ)
+    e.update({k: str(v) for k, v in env.items()})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], capture_output=True, text=True,
+                          timeout=300, cwd=ROOT, env=e)
 
 
-def _worker(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
-                      LOCAL_RANK=str(rank))
-    import torch.distributed as dist
+@pytest.mark.parametrize("args,env", [
+    (["--workload", "tiny"], {"WORLD_SIZE": 2, "RANK": 0, "LOCAL_RANK": 0}),
+    (["--workload", "tiny", "--gpus", "2"], {}),
+], ids=["torchrun_world_2", "gpus_2"])
+def test_gpu_arm_refuses_more_than_one_gpu(args, env):
+    r = _bench(args, **env)
+    assert r.returncode == 2, (r.returncode, r.stderr[-2000:])
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "ours" and d["n_gpus"] == 2 and "one GPU" in d["unavailable"]
+    # refused before the library was loaded or a kernel was built
+    assert "libflce" not in r.stderr and "Traceback" not in r.stderr
 
-    import bench
-    w, r, _ = bench.dist_setup(world)
-    assert (w, r) == (world, rank)
-    bench.barrier(w)
-    out[rank] = bench.max_over_ranks(10.0 * (rank + 1), w)
-    dist.destroy_process_group()
+
+def test_gpu_arm_refusal_is_quiet_on_other_ranks():
+    r = _bench(["--workload", "tiny"], WORLD_SIZE=2, RANK=1, LOCAL_RANK=1)
+    assert r.returncode == 2 and not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
 
 
-def test_two_gloo_ranks_take_the_max_time():
-    ctx = mp.get_context("spawn")
-    mgr = ctx.Manager()
-    out = mgr.dict()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=120)
-        assert p.exitcode == 0
-    assert dict(out) == {0: 20.0, 1: 20.0}
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _bench(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "0"], WORLD_SIZE=2,
+               RANK=1, LOCAL_RANK=1)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_bench_makes_no_process_group():
+    """No collective, no NCCL: bench.py never creates a process group."""
+    src = open(os.path.join(ROOT, "bench.py")).read()
+    assert "init_process_group" not in src and "torch.distributed" not in src
 
 
 def test_launch_count_matches_the_band_schedule():
@@ -75,12 +83,7 @@ def test_reference_arm_prints_the_contract_line():
     """bench.py --impl reference (the fp64 oracle on the host cores) prints one JSON line
     with the contract's keys, its cpu_baseline describing the same run, and an e2e with no
     host-device bytes."""
-    import json
-    import subprocess
-    import sys
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
-                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=root)
+    r = _bench(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"])
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -94,3 +97,6 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    # the time per step is the time of what ran: rows_per_step rows at the line's rate
+    rows = d["config"]["rows_per_step"]
+    assert abs(d["ms_per_step"] * d["value"] / 1000.0 - rows) <= 1e-6 * rows

@@ -156,6 +156,21 @@ def make_inputs(wl: Workload, seed: int | None = None, dtype: torch.dtype = torc
     return X, W, y
 
 
+def make_targets_of(wl: Workload, seed: int | None = None) -> torch.Tensor:
+    """The targets (with the ignore mask) that make_inputs draws for this workload and
+    seed, without drawing X and W."""
+    root = np.random.SeedSequence(wl.seed if seed is None else seed)
+    _, _, sy = root.spawn(3)
+    return make_targets(wl, sy)
+
+
+# The shape of the peak-memory comparison in "Cutting LLM Memory by 84%: A Deep Dive into
+# Fused Kernels", section "Memory Benchmark": one 16,384-token sequence through the
+# Llama-3-8B head (D=4096, V=128,256). The page used real text; uniform targets stand in.
+MEMORY_BENCHMARK = Workload("memory_benchmark", 16384, 4096, 128256, seed=5,
+                            note="peak-memory shape of the Memory Benchmark section, uniform targets, mean")
+
+
 def custom(name: str, N: int, D: int, V: int, seed: int = 0, **kw) -> Workload:
     """A workload with the same recipe and other shapes (parity edge cases)."""
     return Workload(name, N, D, V, seed=seed, **kw)

@@ -24,6 +24,11 @@ CASES = [
     # ignore_index that is also a class id, near-total smoothing, a strong z-loss
     ("unusual_options", custom("odd", 333, 72, 1544, seed=22, ignore_frac=0.1, ignore_index=0,
                                label_smoothing=0.999, zloss_scale=1.0)),
+    # a vocabulary of 8 or 16 with heavy smoothing: each non-target column gets eps/V of the
+    # target mass, so spreading it over V-1 columns instead is ~7% of a gradient entry
+    ("small_vocab_smoothing_mean", custom("v8s", 512, 64, 8, seed=23, ignore_frac=0.1, label_smoothing=0.5)),
+    ("small_vocab_smoothing_sum", custom("v16s", 512, 64, 16, seed=24, ignore_frac=0.1, label_smoothing=0.9,
+                                         reduction="sum")),
 ]
 
 

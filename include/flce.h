@@ -54,8 +54,10 @@
  * Errors: host-side argument checks return a status synchronously and launch
  * nothing. Conditions found on the device (a target outside [0, V) that is not
  * the ignore index; a pipeline wait that exceeded its time limit) set an error
- * word inside the workspace and poison the affected results with NaN; no kernel
- * traps. flce_check_device_error reads that word.
+ * word inside the workspace and poison the affected results with NaN (a bad target:
+ * its row's loss and gradient rows; a timeout: every lse and loss value of the
+ * forward, every element of a 16-bit dX of the backward, while dW is then undefined);
+ * no kernel traps. flce_check_device_error reads that word.
  *
  * Requirements: a compute capability 10.3 device (GB300); D % 8 == 0 and
  * V % 8 == 0 (16-byte row strides for the tensor-memory-access unit); X, W, dX,
@@ -298,15 +300,21 @@ flce_status flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, struct 
  * device arena and forbid further allocation). The source pages have no
  * counterpart: this is a library convenience. Arguments, outputs and results are
  * those of flce_forward; the scratch is a 64 MiB device array inside the library,
- * taken on every GPU where this entry point is used until the process exits.
+ * taken on every GPU where this entry point is used until the process exits (under
+ * CUDA's default lazy module loading; with CUDA_MODULE_LOADING=EAGER it is taken on
+ * every device the process uses).
  *  - The first call on a device (with that device current) looks up the array's
- *    device address; make that first call before any stream capture.
+ *    device address and keeps it; make that first call before any stream capture,
+ *    and do not use this entry point after a device reset (the kept address would be
+ *    stale).
  *  - All calls share the array: calls that overlap on the GPU race; serialise them.
  *    Each call clears the parts that must start at zero.
  *  - Shapes needing more than 64 MiB of forward scratch (flce_workspace_size(N, D,
  *    V, 0)) return FLCE_ERR_WORKSPACE_TOO_SMALL and launch nothing.
- *  - It never calls cudaMalloc, cudaFree or any allocating routine. Device-detected
- *    bad targets still poison the loss with NaN; the error word is internal. */
+ *  - It never calls cudaMalloc, cudaFree or any allocating routine.
+ *  - Its device error word is internal, so device findings show in the results: a bad
+ *    target makes its row's loss (and the reduced loss) NaN, and a pipeline wait that
+ *    ran out makes every lse and loss value of the call NaN. */
 flce_status flce_forward_noalloc(const void* X, const void* W, const int32_t* targets,
                                  int64_t N, int64_t D, int64_t V, int32_t ignore_index,
                                  float label_smoothing, float zloss_scale, flce_reduction red,

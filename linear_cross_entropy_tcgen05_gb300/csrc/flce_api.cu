@@ -762,11 +762,11 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, pb.f16, stream));
     }
     if (compact) {
-      const ScatterCastParams sc{dx_acc, dXrows, slot, int(nb), int(pb.D), pb.f16 ? 1 : 0};
+      const ScatterCastParams sc{dx_acc, dXrows, slot, int(nb), int(pb.D), pb.f16 ? 1 : 0, err};
       FLCE_CUDA_CHECK(launch_scatter_cast(sc, sms, stream));
     } else if (!f32_out) {
       void* dXb = static_cast<uint8_t*>(dX) + size_t(n0) * size_t(pb.D) * 2;
-      FLCE_CUDA_CHECK(launch_cast_16bit(dx_acc, dXb, size_t(nb) * size_t(pb.D), pb.f16, sms, stream));
+      FLCE_CUDA_CHECK(launch_cast_16bit(dx_acc, dXb, size_t(nb) * size_t(pb.D), pb.f16, sms, err, stream));
     }
   }
   return FLCE_OK;

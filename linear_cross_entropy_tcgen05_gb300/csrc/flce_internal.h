@@ -120,6 +120,7 @@ struct ScatterCastParams {
   const int* slot;
   int N, D;
   int f16;
+  const int* err;     // the call's error word: a pipeline timeout makes every dX element NaN
 };
 
 // Sentinel target of an ignored row in the per-row gradient coefficients.
@@ -277,7 +278,8 @@ cudaError_t launch_dw_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 cudaError_t launch_dx_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const WalkParams& w, const StoreEpiParams& e, bool w_vd, bool f16, cudaStream_t stream);
 // fp32 -> bf16 (or f16) of n elements, n a multiple of 4.
-cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream);
+cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, const int* err,
+                              cudaStream_t stream);
 // Valid-row compaction of the backward: the list of valid rows and their count (one
 // block), the gather of their X rows and coefficients, and the final cast of the
 // compacted dX accumulator back to the original rows.

@@ -13,10 +13,18 @@
 // Properties:
 //  * The array takes 64 MiB of device memory on every GPU where it is used, from the
 //    first call on that GPU (when CUDA loads this module) until the process exits.
+//    That holds under CUDA's default lazy module loading; with
+//    CUDA_MODULE_LOADING=EAGER the module, and so the array, is loaded on every device
+//    the process uses, whether or not this entry point is ever called.
 //  * The first call on a device, with that device current, looks the array's
 //    device address up with cudaGetSymbolAddress (the host-side name of a
-//    __device__ array is only a stand-in, never a device pointer). Make that first
-//    call before any stream capture.
+//    __device__ array is only a stand-in, never a device pointer) and keeps it for the
+//    life of the process. Make that first call before any stream capture. A device
+//    reset (cudaDeviceReset, or a primary context released and created again) makes
+//    the kept address stale: do not use this entry point after one.
+//  * Its error word is internal. A bad target gives that row's loss (and the reduced
+//    loss) NaN, as in flce_forward; a pipeline wait that ran out gives NaN in every lse
+//    and loss value of the call.
 //  * Every call on a device shares the one array and it keeps the previous call's
 //    contents. Each call clears what must start at zero (the error word) itself; all
 //    other scratch is fully overwritten. Calls whose execution overlaps on the GPU

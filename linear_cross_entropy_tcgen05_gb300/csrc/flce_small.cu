@@ -25,9 +25,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 // vocabulary shard's statistics (FIN_SHARD_STATS), or combine K shards' statistics
 // (FIN_COMBINE); then reduce the loss deterministically (per-block fp64 partial sums,
 // then one block).
+// A forward GEMM whose pipeline wait ran out has set FLCE_DEVERR_TIMEOUT in this call's
+// error word (cleared when the call began) and left its partial statistics unwritten; they
+// may hold a previous call's values, so every result of this call is NaN instead.
+__device__ __forceinline__ bool forward_timed_out(const int* err) {
+  return err != nullptr && (*reinterpret_cast<const volatile int*>(err) & FLCE_DEVERR_TIMEOUT) != 0;
+}
+
 __global__ void __launch_bounds__(kFinalizeThreads)
     flce_finalize_rows_kernel(const FinalizeParams p) {
   const int row = int(blockIdx.x) * kFinalizeThreads + int(threadIdx.x);
+  const bool timed_out = forward_timed_out(p.err);
   double contrib = 0.0, den = 0.0;
   int valid = 0, correct = 0;
   if (row < p.N) {
@@ -62,14 +70,14 @@ __global__ void __launch_bounds__(kFinalizeThreads)
       }
       zy = p.tgt[row];
     }
-    const float lse = M + logf(d);
+    const float lse = timed_out ? CUDART_NAN_F : M + logf(d);
     const int y = p.targets[row];
     if (p.mode == FIN_SHARD_STATS) {
       const int rel = y - p.v_offset;
       const bool own = y != p.ignore_index && rel >= 0 && rel < p.V_local;
       p.stats_out[row] = lse;
-      p.stats_out[size_t(p.N) + row] = sz;
-      p.stats_out[2 * size_t(p.N) + row] = own ? zy : 0.f;
+      p.stats_out[size_t(p.N) + row] = timed_out ? CUDART_NAN_F : sz;
+      p.stats_out[2 * size_t(p.N) + row] = timed_out ? CUDART_NAN_F : (own ? zy : 0.f);
       p.stats_out[3 * size_t(p.N) + row] = own ? 1.f : 0.f;
       return;
     }
@@ -92,6 +100,7 @@ __global__ void __launch_bounds__(kFinalizeThreads)
         correct = (p.predicted != nullptr && best_idx == y) ? 1 : 0;
       }
     }
+    if (timed_out) ell = CUDART_NAN_F;
     if (p.reduction == 2) p.loss[row] = ell;
     contrib = double(ell);
   }
@@ -152,12 +161,14 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     __syncthreads();
   }
   if (threadIdx.x == 0) {
+    const bool timed_out = forward_timed_out(p.err);
     if (p.reduction != 2) {
       double total = ssum[0];
       if (p.reduction == 0) total = sden[0] != 0.0 ? total / sden[0] : 0.0;
-      p.loss[0] = float(total);
+      p.loss[0] = timed_out ? CUDART_NAN_F : float(total);
     }
-    if (p.accuracy != nullptr) p.accuracy[0] = scnt[0] ? float(double(scor[0]) / double(scnt[0])) : 0.f;
+    if (p.accuracy != nullptr)
+      p.accuracy[0] = timed_out ? CUDART_NAN_F : (scnt[0] ? float(double(scor[0]) / double(scnt[0])) : 0.f);
   }
 }
 
@@ -286,10 +297,14 @@ __device__ __forceinline__ uint2 pack4_16bit(const float4 v) {
   }
 }
 
+// A backward GEMM whose pipeline wait ran out leaves parts of the dX accumulator
+// unwritten: the casts then write NaN to every dX element of the call.
 template <bool F16>
-__global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+__global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4, const int* err) {
+  const bool timed_out = forward_timed_out(err);
+  const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x)
-    dst[i] = pack4_16bit<F16>(src[i]);
+    dst[i] = pack4_16bit<F16>(timed_out ? nan4 : src[i]);
 }
 
 // ---------------------------------------------------------------------------------
@@ -366,11 +381,14 @@ __global__ void __launch_bounds__(256) flce_scatter_cast_kernel(const ScatterCas
   const int lane = int(threadIdx.x) & 31;
   const int warps = int(gridDim.x) * (int(blockDim.x) >> 5);
   const int n4 = p.D / 4;
+  const bool timed_out = forward_timed_out(p.err);
+  const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
   for (int r = int(blockIdx.x) * (int(blockDim.x) >> 5) + (int(threadIdx.x) >> 5); r < p.N; r += warps) {
     const int sl = p.slot[r];
     const float4* from = reinterpret_cast<const float4*>(p.acc) + size_t(sl < 0 ? 0 : sl) * size_t(n4);
     uint2* to = reinterpret_cast<uint2*>(p.dX) + size_t(r) * size_t(n4);
-    for (int c = lane; c < n4; c += 32) to[c] = sl < 0 ? make_uint2(0u, 0u) : pack4_16bit<F16>(from[c]);
+    for (int c = lane; c < n4; c += 32)
+      to[c] = timed_out ? pack4_16bit<F16>(nan4) : (sl < 0 ? make_uint2(0u, 0u) : pack4_16bit<F16>(from[c]));
   }
 }
 
@@ -477,7 +495,8 @@ cudaError_t launch_scatter_cast(const ScatterCastParams& p, int num_sms, cudaStr
   return cudaGetLastError();
 }
 
-cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, cudaStream_t stream) {
+cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, int num_sms, const int* err,
+                              cudaStream_t stream) {
   const size_t n4 = n / 4;
   size_t blocks = (n4 + 255) / 256;
   const size_t cap = size_t(num_sms) * 8;
@@ -485,10 +504,10 @@ cudaError_t launch_cast_16bit(const float* src, void* dst, size_t n, bool f16, i
   if (blocks == 0) blocks = 1;
   if (f16)
     flce_cast_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
-                                                                 reinterpret_cast<uint2*>(dst), n4);
+                                                                 reinterpret_cast<uint2*>(dst), n4, err);
   else
     flce_cast_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
-                                                                  reinterpret_cast<uint2*>(dst), n4);
+                                                                  reinterpret_cast<uint2*>(dst), n4, err);
   count_launch();
   return cudaGetLastError();
 }

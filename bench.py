@@ -114,10 +114,17 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        power = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                power.append(float(f[3]))
+            except (IndexError, ValueError):
+                pass
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-               "samples": len(sm)}
+               "samples": len(sm), "power_w": statistics.median(power) if power else None}
         if getattr(self, "remeasured", False):
             out["remeasured"] = True
         return out
@@ -329,10 +336,25 @@ def run_ours(args, wl):
         if args.only == "bwd":
             pb.fwd()
         step = pb.fwd if args.only == "fwd" else pb.bwd
-        for _ in range(args.warmup + args.steps):
+        for _ in range(args.warmup):
             step()
         torch.cuda.synchronize(dev)
-        line = {"only": args.only, "workload": wl.name}
+        # each call timed with CUDA events on the stream, clocks sampled meanwhile
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        with ClockSampler(0) as clk:
+            for a, b in ev:
+                a.record(stream)
+                step()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) for a, b in ev]
+        c = clk.summary()
+        line = {"only": args.only, "workload": wl.name, "steps": args.steps, "ms_mean": statistics.mean(ms),
+                "ms_median": statistics.median(ms), "clocks": c}
+        if c["sm_mhz"]:
+            # time x clock: the work in SM cycles, comparable across boxes and power states
+            line["mcycles_median"] = statistics.median(ms) * c["sm_mhz"] / 1000.0
         if args.wait_stats:
             line["pipeline_waits"] = pipeline_waits(pb.ws, args.only)
         st = flce.flce_check_device_error(pb.ws, stream)

@@ -3,8 +3,10 @@
 //
 // Forward  ("Cutting LLM Memory by 84%", "Definition and Forward Pass"; Liger-Kernel
 //           PR #1291 "Summary", store-free forward):
-//   1. tensor-core GEMM over (row tile, vocabulary range) units with the online-softmax
-//      epilogue -> partial (max, sum-exp, sum-z) per row and range, target logit;
+//   1. tensor-core GEMM over (cluster row block, vocabulary chunk) units, walked panel by
+//      panel so that concurrent clusters share X rows and W tiles in L2, with the
+//      online-softmax epilogue -> partial (max, sum-exp, sum-z) per row and chunk, target
+//      logit;
 //   2. finalize: combine the partials -> lse, row losses, deterministic reduction.
 // Backward ("Backward Pass" and "Path to Production" of the same post; PR #1291: dW
 //           contracts over the tokens and is written once):
@@ -53,9 +55,6 @@ namespace {
 #ifndef FLCE_L2_PROMOTION
 #define FLCE_L2_PROMOTION 3  // tensor-map L2 promotion: 0 none, 1 64 B, 2 128 B, 3 256 B
 #endif
-#ifndef FLCE_FWD_GN
-#define FLCE_FWD_GN 0  // forward row blocks per group; 0 chooses from the resident CTA pairs
-#endif
 #ifndef FLCE_COMPACT_ROWS
 #define FLCE_COMPACT_ROWS 1  // 1: the backward GEMMs skip ignored rows (valid-row compaction)
 #endif
@@ -73,8 +72,9 @@ struct FwdLayout {
 
 // Header words of every workspace: [0] device error word, [8] number of valid rows
 // (backward compaction), [16] B = g eps / V (backward), [24] sum of the class weights,
-// [28] g (backward).
-constexpr size_t kHdrErr = 0, kHdrNValid = 8, kHdrB = 16, kHdrWtot = 24, kHdrG = 28;
+// [28] g (backward), [192] the forward GEMM's unit ticket counter. Bytes 32..159 hold
+// the pipeline-wait counters of the diagnostic build.
+constexpr size_t kHdrErr = 0, kHdrNValid = 8, kHdrB = 16, kHdrWtot = 24, kHdrG = 28, kHdrTicket = 192;
 
 FwdLayout fwd_layout(int64_t N, int64_t V) {
   FwdLayout L{};
@@ -334,23 +334,17 @@ flce_status check_common(const void* X, const void* W, const int32_t* targets, i
 }
 
 // Forward grid: gN row blocks x S vocabulary ranges = the resident CTA pairs.
-void pick_forward_grid(int units, int64_t n_tiles, int64_t v_tiles, int S_alloc, int* gN_out, int* S_out) {
-  int gN = 1;
-  const int cands[4] = {8, 4, 2, 1};
-  for (int c : cands)
-    if (units % c == 0 && units / c <= kMaxSplits) {
-      gN = c;
-      break;
-    }
-  if (FLCE_FWD_GN > 0 && FLCE_FWD_GN <= units) gN = FLCE_FWD_GN;
-  const int64_t row_blocks = cdiv(cdiv(n_tiles, kFwdRowBlock), gemm_pairs_per_cluster());  // per cluster
-  if (gN > row_blocks) gN = int(row_blocks);
-  int64_t S = units / gN;
-  if (S > v_tiles) S = v_tiles;
-  if (S > S_alloc) S = S_alloc;
-  if (S < 1) S = 1;
-  *gN_out = gN;
-  *S_out = int(S);
+// The forward's units: cluster row blocks x vocabulary chunks (at most kMaxSplits chunks,
+// so at most that many partial statistics per row), walked panel by panel.
+void pick_forward_schedule(int64_t n_tiles, int64_t v_tiles, FwdParams* p) {
+  const int64_t n_blocks = cdiv(n_tiles, int64_t(gemm_pairs_per_cluster()) * kFwdRowBlock);
+  const int64_t chunk_tiles = cdiv(v_tiles, kMaxSplits);
+  const int64_t n_chunks = cdiv(v_tiles, chunk_tiles);
+  p->n_blocks = int(n_blocks);
+  p->panel = int(n_blocks < FLCE_FWD_PANEL ? n_blocks : FLCE_FWD_PANEL);
+  p->chunk_tiles = int(chunk_tiles);
+  p->n_chunks = int(n_chunks);
+  p->total_units = int(n_blocks * n_chunks);
 }
 
 #define FLCE_CUDA_CHECK(expr)                    \
@@ -467,13 +461,11 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
 
 // Forward GEMM + finalize. mode FIN_LOSS (loss, lse, options) or FIN_SHARD_STATS.
 flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, int64_t v_offset, float* loss,
-                        float* lse, float* stats, uint8_t* ws, bool clear_header, int units, cudaStream_t stream) {
+                        float* lse, float* stats, uint8_t* ws, bool clear_header, cudaStream_t stream) {
   const FwdLayout L = fwd_layout(pb.N, pb.V);
   int* err = reinterpret_cast<int*>(ws + kHdrErr);
   float* wtot = reinterpret_cast<float*>(ws + kHdrWtot);
   const int64_t n_tiles = cdiv(pb.N, gemm_tile_rows()), v_tiles = cdiv(pb.V, kBN);
-  int gN = 1, S = 1;
-  pick_forward_grid(units, n_tiles, v_tiles, L.S_alloc, &gN, &S);
 
   // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;
@@ -497,8 +489,9 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   p.V = int(pb.V);
   p.n_tiles = int(n_tiles);
   p.v_tiles = int(v_tiles);
-  p.gN = gN;
-  p.S = S;
+  pick_forward_schedule(n_tiles, v_tiles, &p);
+  p.ticket = reinterpret_cast<int*>(ws + kHdrTicket);  // zeroed with the header above
+  if (!clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(p.ticket, 0, sizeof(int), stream));
   p.num_kb = int(cdiv(pb.D, kBK));
   p.want_sum_z = (mode == FIN_SHARD_STATS) || pb.eps != 0.f;
   p.ignore_index = pb.ignore_index;
@@ -526,7 +519,7 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   f.targets = pb.targets;
   f.N = int(pb.N);
   f.V = int(pb.V);
-  f.S = S;
+  f.S = p.n_chunks;
   f.V_local = int(pb.V);
   f.v_offset = int(v_offset);
   f.ignore_index = pb.ignore_index;
@@ -814,7 +807,7 @@ flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets
     note_error("forward_max_units", "no resident cluster");
     return FLCE_ERR_CUDA;
   }
-  return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), true, units,
+  return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), true,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -884,7 +877,7 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, true, units, s)) != FLCE_OK) return st;
+  if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, true, s)) != FLCE_OK) return st;
   return run_backward(pb, opt, lse, grad_out, dX, dW, ws, false, sms, s);
 }
 
@@ -925,7 +918,7 @@ flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* tar
   }
   const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, opt_w_vd(opt), opt_f16(opt)};
   return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
-                     static_cast<uint8_t*>(workspace), true, units, reinterpret_cast<cudaStream_t>(stream));
+                     static_cast<uint8_t*>(workspace), true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* targets, int64_t N, int64_t v_total,

@@ -107,44 +107,156 @@ __device__ __forceinline__ Pair pair_id() {
 // Tile schedules (every role of both CTAs of a pair walks the same sequence)
 // ---------------------------------------------------------------------------------
 
-// Forward: the clusters form gN row blocks x S vocabulary ranges; a row block is
-// kFwdRowBlock row tiles. Cluster c keeps row-block offset c % gN and walks groups of gN
-// row blocks; in group g it covers vocabulary range (c / gN + g) mod S, so the extra tile
-// of the longer ranges rotates among clusters. For every vocabulary tile of its range the
-// cluster computes the tiles of all row tiles of its block back to back, so each W tile
-// is streamed from HBM once per row block and re-read from L2 right away. Running
-// statistics stay in registers (one set per row tile of the block) and are written once
-// per (row, range).
+// Forward: the work is n_blocks cluster row blocks (each MC pairs x kFwdRowBlock row
+// tiles) times n_chunks vocabulary chunks (chunk_tiles W tiles each). Units are numbered
+// panel by panel (`panel` row blocks), within a panel chunk by chunk, within a chunk
+// block by block, and handed out in that order by a ticket counter: a cluster takes the
+// next unit when its producer has issued the loads of the current one. So the units in
+// work at any time are neighbours in that order however far the clusters drift apart:
+// the rows of one panel of X and the W tiles of a few neighbouring chunks, together well
+// under the L2 share that data read from both dies of the GPU can use (each die keeps its
+// own copy of such lines). Within a unit a pair computes its row tiles back to back
+// against each W tile of the chunk (W multicast to the cluster's pairs); running
+// statistics stay in registers (one set per row tile) and are written once per (row,
+// chunk).
+//
+// The cluster's CTA 0 producer draws the tickets and publishes each unit into a ring of
+// kUnitRing slots in the shared memory of every CTA of the cluster (a cluster store, then
+// a release-arrive on the slot's `full` barrier). The other producers and the MMA threads
+// read the slot after an acquire-wait; in the epilogue one thread waits and hands the unit
+// to the other 127 through shared memory behind the epilogue's named barrier, so that all
+// of them take the same path. Each reader releases the slot on CTA 0's `empty` barrier,
+// which the ticket producer waits on before it reuses the slot. Unit -1 ends the walk;
+// -2 means a wait gave up (the CTA is aborting).
+constexpr int kUnitRing = 16;
+constexpr int kUnitBytes = 512;  // full[16], empty[16] barriers, 16 slots, the epilogue's copy
+
+template <int CG, int MC>
+__host__ __device__ constexpr uint32_t unit_consumers() {
+  // producers of CTAs 1.., the MMA thread of each pair, one epilogue thread of each CTA
+  return uint32_t(CG * MC - 1 + MC + CG * MC);
+}
+
+enum UnitRole : int { UNIT_TICKETS = 0, UNIT_THREAD = 1, UNIT_EPILOGUE = 2 };
+
+struct UnitRing {
+  uint64_t* full;  // [kUnitRing] (every CTA)
+  uint64_t* empty; // [kUnitRing] (waited on in CTA 0)
+  int* slot;       // [kUnitRing]
+  int* epi_unit;   // the epilogue's copy of its current unit
+};
+
+// `bars`: the start of the barrier region (the stage barriers).
+__device__ __forceinline__ UnitRing carve_units(uint64_t* bars) {
+  uint8_t* base = reinterpret_cast<uint8_t*>(bars) + kBarrierBytes;
+  UnitRing u;
+  u.full = reinterpret_cast<uint64_t*>(base);
+  u.empty = u.full + kUnitRing;
+  u.slot = reinterpret_cast<int*>(u.empty + kUnitRing);
+  u.epi_unit = u.slot + kUnitRing;
+  return u;
+}
+
+struct FwdSchedArgs {
+  const FwdParams* p;
+  UnitRing ring;
+  WaitCtx w;
+  int role;
+};
+
 template <int CG, int MC>
 struct FwdSched {
-  int n_tiles, v_tiles, gN, S, num_kb;
-  int n_off, split, rank, pair;
-  int g, vt, vt0, vt_end, range, rb0, rb_tiles, j;
+  int n_tiles, v_tiles, n_blocks, panel, chunk_tiles, n_chunks, total_units, num_kb;
+  int* ticket;
+  UnitRing ring;
+  WaitCtx w;
+  int role, k, rank, pair;
+  bool gave_up;
+  int vt, vt0, vt_end, chunk, rb0, rb_tiles, j;
 
-  __device__ explicit FwdSched(const FwdParams& p) : n_tiles(p.n_tiles), v_tiles(p.v_tiles), gN(p.gN), S(p.S),
-                                                     num_kb(p.num_kb) {
+  __device__ explicit FwdSched(const FwdSchedArgs& a)
+      : n_tiles(a.p->n_tiles), v_tiles(a.p->v_tiles), n_blocks(a.p->n_blocks), panel(a.p->panel),
+        chunk_tiles(a.p->chunk_tiles), n_chunks(a.p->n_chunks), total_units(a.p->total_units),
+        num_kb(a.p->num_kb), ticket(a.p->ticket), ring(a.ring), w(a.w), role(a.role) {
     const Pair pr = pair_id<CG, MC>();
-    n_off = pr.cid % gN;
-    split = pr.cid / gN;
     rank = pr.rank;
     pair = pr.pair;
-    g = -1;
-    vt = vt0 = vt_end = range = rb0 = rb_tiles = j = 0;
+    k = 0;
+    gave_up = false;
+    vt = vt0 = vt_end = chunk = rb0 = rb_tiles = j = 0;
+  }
+
+  // A wait for a unit gave up: the calling role drains what it has issued.
+  __device__ bool aborted() const { return gave_up; }
+
+  // The k-th unit of this cluster (-1: no more; -2: a wait gave up).
+  __device__ int next_unit() {
+    if (role == UNIT_EPILOGUE) {
+      const int epi_tid = int(threadIdx.x) - 64;
+      if (epi_tid == 0) *reinterpret_cast<volatile int*>(ring.epi_unit) = read_unit();
+      named_barrier_sync(1, kEpiThreads);
+      return *reinterpret_cast<volatile int*>(ring.epi_unit);
+    }
+    return read_unit();
+  }
+
+  __device__ int read_unit() {
+    constexpr int kCtas = CG * MC;
+    const int slot = k % kUnitRing;
+    const uint32_t use = uint32_t(k / kUnitRing);
+    ++k;
+    if (role == UNIT_TICKETS) {
+      if (use > 0 && !mbar_wait(&ring.empty[slot], (use - 1u) & 1u, w)) return -2;  // every reader is done
+      int t = atomicAdd(ticket, 1);
+      if (t >= total_units) t = -1;
+      const uint32_t sa = smem_addr(&ring.slot[slot]), fa = smem_addr(&ring.full[slot]);
+#pragma unroll
+      for (int r = 0; r < kCtas; ++r) {
+        if (kCtas == 1) {
+          *reinterpret_cast<volatile int*>(&ring.slot[slot]) = t;
+          mbar_arrive(&ring.full[slot]);
+        } else {
+          st_shared_cluster_u32(map_shared_to_rank(sa, uint32_t(r)), uint32_t(t));
+          mbar_arrive_cluster(map_shared_to_rank(fa, uint32_t(r)));
+        }
+      }
+      return t;
+    }
+    if (!mbar_wait_acq_cluster(&ring.full[slot], use & 1u, w)) return -2;
+    const int t = *reinterpret_cast<volatile int*>(&ring.slot[slot]);
+    if (kCtas == 1)
+      mbar_arrive(&ring.empty[slot]);
+    else
+      mbar_arrive_cluster(map_shared_to_rank(smem_addr(&ring.empty[slot]), 0u));
+    return t;
   }
 
   __device__ bool next(Tile& t) {
     if (vt >= vt_end) {
-      ++g;
-      // the cluster's MC row blocks; the pairs walk in lockstep, so a pair whose block
-      // runs past the last row tile computes zero rows (loads beyond N read zeros)
-      const int cluster_rb0 = (g * gN + n_off) * MC * kFwdRowBlock;
-      if (cluster_rb0 >= n_tiles) return false;
-      rb0 = cluster_rb0 + pair * kFwdRowBlock;
+      const int u = next_unit();
+      if (u == -2) gave_up = true;
+      if (u < 0) return false;
+      // unit -> (panel, chunk, block within the panel); the last panel may be narrower
+      const int per_panel = panel * n_chunks;
+      const int full = n_blocks / panel;
+      int blk;
+      if (u < full * per_panel) {
+        const int pn = u / per_panel;
+        const int r = u - pn * per_panel;
+        chunk = r / panel;
+        blk = pn * panel + (r - chunk * panel);
+      } else {
+        const int last = n_blocks - full * panel;
+        const int r = u - full * per_panel;
+        chunk = r / last;
+        blk = full * panel + (r - chunk * last);
+      }
+      // the pairs walk in lockstep, so a pair whose block runs past the last row tile
+      // computes zero rows (loads beyond N read zeros)
+      rb0 = (blk * MC + pair) * kFwdRowBlock;
       rb_tiles = (MC > 1 || n_tiles - rb0 >= kFwdRowBlock) ? kFwdRowBlock : n_tiles - rb0;
-      range = (split + g) % S;
-      vt0 = vt = int((long long)range * v_tiles / S);
-      vt_end = int((long long)(range + 1) * v_tiles / S);
-      if (vt >= vt_end) return false;  // S <= v_tiles on the host, so never taken
+      vt0 = vt = chunk * chunk_tiles;
+      vt_end = min(v_tiles, vt0 + chunk_tiles);
       j = 0;
     }
     t.a_row = (rb0 + j) * Geo<CG>::kTileRows + rank * kBM;
@@ -152,7 +264,7 @@ struct FwdSched {
     t.a_k0 = 0;
     t.b_k0 = 0;
     t.num_kb = num_kb;
-    t.aux = range;
+    t.aux = chunk;
     t.sub = j;
     t.flags = (vt == vt0 ? TILE_FIRST : 0) | (vt + 1 == vt_end ? TILE_LAST : 0);
     if (++j == rb_tiles) {
@@ -195,6 +307,8 @@ struct WalkSched {
       }
     }
   }
+  __device__ bool aborted() const { return false; }
+
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;
     const int major = i / w.tiles_minor;
@@ -443,6 +557,7 @@ __device__ __forceinline__ void producer_role(const Smem& s, const CUtensorMap* 
       if (++stage == STAGES) { stage = 0; phase ^= 1u; }
     }
   }
+  if (sched.aborted()) ok = false;
 #if FLCE_WAIT_STATS
   if (leader) atomicAdd(reinterpret_cast<unsigned long long*>(w.err_word + 8 + 8 * (KIND + 1)) + 2, t_empty);
 #endif
@@ -505,6 +620,7 @@ __device__ __forceinline__ void mma_role(const Smem& s, uint32_t tmem_base, cons
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
+  if (sched.aborted()) ok = false;
 #if FLCE_WAIT_STATS
   {
     unsigned long long* st = reinterpret_cast<unsigned long long*>(w.err_word + 8 + 8 * (KIND + 1));
@@ -677,7 +793,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Pair pr = pair_id<CG, MC>();
   const int rank = pr.rank;
 
-  if (threadIdx.x == 0) init_barriers<CG, MC, STAGES>(s);
+  const UnitRing ring = carve_units(s.full);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&ring.full[i], 1);
+      mbar_init(&ring.empty[i], unit_consumers<CG, MC>());
+    }
+    init_barriers<CG, MC, STAGES>(s);  // ends with the barrier-init fence
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -685,17 +808,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_setup<CG, MC>(s, warp);
   const uint32_t tmem_base = *s.tmem_slot;
   const WaitCtx w{s.abort_flag, p.err};
+  const int cta = (CG * MC == 1) ? 0 : int(cluster_ctarank());
 
   if (warp == 0) {
-    if (lane == 0) producer_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, p, w, pr);
+    if (lane == 0) {
+      const FwdSchedArgs a{&p, ring, w, cta == 0 ? UNIT_TICKETS : UNIT_THREAD};
+      producer_role<CG, MC, STAGES, false, B_MN, KIND_FWD, FwdSched<CG, MC>>(s, &tmA, &tmB, a, w, pr);
+    }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0)
-      mma_role<CG, MC, STAGES, false, B_MN, F16, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, p, w, pr.leader);
+    if (lane == 0 && rank == 0) {
+      const FwdSchedArgs a{&p, ring, w, UNIT_THREAD};
+      mma_role<CG, MC, STAGES, false, B_MN, F16, KIND_FWD, FwdSched<CG, MC>>(s, tmem_base, a, w, pr.leader);
+    }
   } else {
     const int epi_tid = int(threadIdx.x) - 64;
     const int r = 32 * (warp & 3) + int(lane);  // TMEM lane = tile row
     const uint32_t lane_addr = tmem_base + (uint32_t(32 * (warp & 3)) << 16);
-    FwdSched<CG, MC> sched(p);
+    FwdSched<CG, MC> sched(FwdSchedArgs{&p, ring, w, UNIT_EPILOGUE});
     Tile t;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -1043,7 +1172,7 @@ auto dw_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, true, tru
 template <bool B_MN, bool F16>
 auto dx_kernel() { return flce_walk_gemm_kernel<kCG, kMC, kWalkStages, false, B_MN, F16, WALK_DX, 1, false>; }
 
-constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>();
+constexpr size_t kFwdSmem = smem_bytes<kCG, kFwdStages, 0>() + kUnitBytes;
 constexpr size_t kWalkSmem = smem_bytes<kCG, kWalkStages, 2>();
 static_assert(kFwdSmem <= 232448 && kWalkSmem <= 232448, "shared memory per CTA");
 
@@ -1102,7 +1231,10 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   cudaError_t e = prepare(kern, kFwdSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = make_config(p.gN * p.S * kCG * kMC, kFwdSmem, stream, attr);
+  const int maxc = max_clusters(kern, kFwdSmem, 0);
+  if (maxc <= 0) return cudaErrorInvalidConfiguration;
+  const int clusters = p.total_units < maxc ? p.total_units : maxc;
+  cudaLaunchConfig_t cfg = make_config(clusters * kCG * kMC, kFwdSmem, stream, attr);
   count_launch();
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }

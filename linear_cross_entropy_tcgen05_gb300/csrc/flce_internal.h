@@ -28,13 +28,22 @@ constexpr int kStagingBytes = 128 * 128;        // one 128-row x 128-byte epilog
 constexpr int kBarrierBytes = 256;
 
 // Forward split of the vocabulary: at most this many partial (max, sum-exp, sum-z)
-// triples per row.
-constexpr int kMaxSplits = 64;
+// triples per row (one per vocabulary chunk of the forward's units).
+#ifndef FLCE_FWD_MAX_SPLITS
+#define FLCE_FWD_MAX_SPLITS 64
+#endif
+constexpr int kMaxSplits = FLCE_FWD_MAX_SPLITS;
 // Forward: row tiles a CTA pair computes against each W tile before moving on.
 #ifndef FLCE_FWD_ROW_BLOCK
-#define FLCE_FWD_ROW_BLOCK 4
+#define FLCE_FWD_ROW_BLOCK 1
 #endif
 constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
+// Forward: cluster row blocks per panel. The clusters working at one time take the
+// blocks of one panel through neighbouring vocabulary chunks, so they share the panel's
+// rows of X and the chunks' W tiles through L2.
+#ifndef FLCE_FWD_PANEL
+#define FLCE_FWD_PANEL 8
+#endif
 // Diagnostic build: the GEMMs add the cycles their MMA thread waited for operands and
 // for the epilogue, its total cycles, and the cycles their producer waited for free
 // stages, to four uint64 counters at bytes 32 + 32 * (kind + 1) of the workspace header
@@ -130,8 +139,13 @@ struct FwdParams {
   const int32_t* targets;
   int N, V;
   int n_tiles, v_tiles;
-  int gN, S;       // grid = gN row tiles x S vocabulary ranges (CTA pairs)
-  int num_kb;      // K blocks over D
+  int n_blocks;     // cluster row blocks (MC pairs x kFwdRowBlock row tiles each)
+  int panel;        // cluster row blocks per panel
+  int chunk_tiles;  // vocabulary tiles per chunk; one partial statistic per row and chunk
+  int n_chunks;     // chunks over the vocabulary (at most kMaxSplits)
+  int total_units;  // n_blocks x n_chunks units, handed out in order by a ticket counter
+  int* ticket;      // the counter (zero when the launch starts)
+  int num_kb;       // K blocks over D
   int want_sum_z;  // label smoothing needs sum_j z_ij
   int ignore_index;
   int y_offset;    // vocabulary shard: global index of W's first column

@@ -271,6 +271,43 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Store a 32-bit word into the shared memory of this CTA or a peer (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// try_wait with cluster-scope acquire: data a peer CTA stored before its release-arrive on
+// this barrier is visible once the phase has completed.
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait as mbar_wait, with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  const uint32_t a = smem_addr(bar);
+  if (mbar_try_wait_acq_cluster(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_acq_cluster(a, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (global_timer_ns() - t0 > FLCE_WAIT_LIMIT_NS) {
+      *w.abort_flag = 1;
+      atomicOr(w.err_word, FLCE_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Global -> this CTA's shared memory; completion bytes counted on an mbarrier that may
 // live in either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr, int x,

@@ -151,8 +151,9 @@ def refuse_multi_gpu(args, world: int, rank: int) -> int:
     return 2
 
 
-def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band=0):
-    """Kernels the library launches per step: forward GEMM + finalize (+ loss reduction),
+def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band=0, compact_fwd=True):
+    """Kernels the library launches per step: (the forward's valid-row list and gather, with
+    a workspace that has room for them) forward GEMM + finalize (+ loss reduction),
     backward denominator, then per row band (one, or ceil(N / row_band)) row coefficients
     (+ valid-row compaction and gather) + 3 GEMMs per vocabulary band + the dX cast. vc is
     the band width (flce_backward_band_width on the device); without it, the workspace's
@@ -164,7 +165,7 @@ def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band
         half = (((V + 1) // 2) + unit - 1) // unit * unit
         vc = min(vc, half)
     bands = -(-V // vc)
-    fwd = 1 + 1 + (0 if reduction == "none" else 1)
+    fwd = (2 if compact_fwd else 0) + 1 + 1 + (0 if reduction == "none" else 1)
     bwd = 1 + -(-N // rows) * (1 + (2 if compact else 0) + 3 * bands + 1)
     return fwd + bwd, bands, vc
 
@@ -391,7 +392,8 @@ def run_ours(args, wl):
     return finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
                   e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width, side,
                   flce.flce_workspace_size(N, D, V, False),
-                  flce.flce_workspace_size(args.row_band if 0 < args.row_band < N else N, D, V, True))
+                  flce.flce_workspace_size(args.row_band if 0 < args.row_band < N else N, D, V, True),
+                  flce.flce_workspace_size(N, D, V, "forward_valid_rows"))
 
 
 def run_e2e(args, dev, stream, X, W, y, pb):
@@ -542,7 +544,7 @@ def run_side_workloads(args, flce, dev, stream):
 
 
 def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes, e2e_value, e2e_ms,
-           h2d, d2h, clk, launches_timed, band_width, side, ws_f, ws_b):
+           h2d, d2h, clk, launches_timed, band_width, side, ws_f, ws_b, ws_fc):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -552,7 +554,8 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
     burst = float(peaks["bf16_tflops"])
     sustained = float(peaks.get("bf16_tflops_sustained", burst))
     launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width,
-                                                   row_band=args.row_band if 0 < args.row_band < N else 0)
+                                                   row_band=args.row_band if 0 < args.row_band < N else 0,
+                                                   compact_fwd=max(ws_f, ws_b) >= ws_fc)
     cpu = None
     if not args.no_cpu_baseline:
         rate, rows, dt = oracle_sample_for(wl, X, W, y, args.cpu_seconds)

@@ -105,7 +105,12 @@ typedef enum {
  * (for_backward == 1) or flce_forward_backward (for_backward == 2) needs for this
  * shape. Returns 0 for invalid sizes. The backward workspace holds a 16-bit gradient
  * band of N x Vc columns (Vc a multiple of 512, at most 16384, and below V once V
- * exceeds 512) and an fp32 [N, D] dX accumulator; no buffer has N x V elements. */
+ * exceeds 512) and an fp32 [N, D] dX accumulator; no buffer has N x V elements.
+ * for_backward == 3 gives the size from which flce_forward (without the argmax and
+ * epilogue options) runs its GEMM on the valid rows only, gathered into the workspace:
+ * the forward's own size plus the row list and the valid rows of X (N x D 16-bit values).
+ * Any backward or fused workspace has that room. The results are the same either way,
+ * bit for bit; only the time differs. */
 size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward);
 
 /* Forward pass. [P1] "Definition and Forward Pass" and "Kernel Implementation"
@@ -115,8 +120,11 @@ size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward);
  *   ignore_index  : rows whose target equals it have loss 0 (default -100 in [P1]).
  *   label_smoothing in [0,1), zloss_scale >= 0, red : see the definitions above.
  *   loss          : out, fp32 [1] (MEAN/SUM) or [N] (NONE).
- *   lse           : out, fp32 [N], log-sum-exp of every row (ignored rows included).
- *   workspace     : device scratch of at least flce_workspace_size(N,D,V,0) bytes.
+ *   lse           : out, fp32 [N], log-sum-exp of every valid row; 0 for a row whose
+ *                   target is the ignore index (its loss needs no lse; [P1]'s kernel
+ *                   returns early for such rows).
+ *   workspace     : device scratch of at least flce_workspace_size(N,D,V,0) bytes; from
+ *                   flce_workspace_size(N,D,V,3) bytes the GEMM skips the ignored rows.
  * Returns FLCE_OK or a host-side error; nothing is launched on error. */
 flce_status flce_forward(const void* X, const void* W, const int32_t* targets,
                          int64_t N, int64_t D, int64_t V, int32_t ignore_index,

@@ -184,8 +184,20 @@ def flce_last_error_detail() -> str:
     return load_library().flce_last_error_detail().decode()
 
 
-def flce_workspace_size(N: int, D: int, V: int, for_backward: bool) -> int:
-    return int(load_library().flce_workspace_size(N, D, V, 1 if for_backward else 0))
+WORKSPACE_KINDS = {"forward": 0, "backward": 1, "both": 2, "forward_valid_rows": 3}
+
+
+def flce_workspace_size(N: int, D: int, V: int, for_backward) -> int:
+    """Workspace bytes: for_backward False/True (forward / backward), or one of
+    WORKSPACE_KINDS by name or number ("forward_valid_rows": the size from which the
+    forward runs its GEMM on the valid rows only)."""
+    if isinstance(for_backward, str):
+        which = WORKSPACE_KINDS[for_backward]
+    elif isinstance(for_backward, bool):
+        which = 1 if for_backward else 0
+    else:
+        which = int(for_backward)
+    return int(load_library().flce_workspace_size(N, D, V, which))
 
 
 def logits_bytes(N: int, V: int, elem_bytes: int) -> int:

@@ -97,6 +97,23 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
   return L;
 }
 
+// With room for it (flce_workspace_size(..., 3) bytes: any backward workspace has it), the
+// forward runs its GEMM on the valid rows only: the row list, each row's slot, and the
+// valid rows of X gathered (then zero rows up to the padding) follow the forward layout.
+struct FwdCompactLayout {
+  size_t rows, slot, xc, total;
+};
+
+FwdCompactLayout fwd_compact_layout(int64_t N, int64_t D, int64_t V) {
+  FwdCompactLayout C{};
+  size_t o = fwd_layout(N, V).total;
+  C.rows = o; o += align256(size_t(N) * sizeof(int));
+  C.slot = o; o += align256(size_t(N) * sizeof(int));
+  C.xc = o; o += align256(size_t(N) * size_t(D) * 2);
+  C.total = o;
+  return C;
+}
+
 constexpr int kColsumChunks = 64;
 
 struct BwdLayout {
@@ -403,6 +420,7 @@ size_t flce_workspace_size(int64_t N, int64_t D, int64_t V, int for_backward) {
   const size_t f = fwd_layout(N, V).total, b = bwd_layout(N, D, V).total;
   if (for_backward == 0) return f;
   if (for_backward == 1) return b;
+  if (for_backward == 3) return fwd_compact_layout(N, D, V).total;
   return f > b ? f : b;
 }
 
@@ -461,11 +479,17 @@ flce_status check_options(const flce_options* o, const Problem& pb, bool backwar
 
 // Forward GEMM + finalize. mode FIN_LOSS (loss, lse, options) or FIN_SHARD_STATS.
 flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, int64_t v_offset, float* loss,
-                        float* lse, float* stats, uint8_t* ws, bool clear_header, cudaStream_t stream) {
+                        float* lse, float* stats, uint8_t* ws, size_t ws_bytes, bool clear_header, int sms,
+                        cudaStream_t stream) {
   const FwdLayout L = fwd_layout(pb.N, pb.V);
   int* err = reinterpret_cast<int*>(ws + kHdrErr);
   float* wtot = reinterpret_cast<float*>(ws + kHdrWtot);
   const int64_t n_tiles = cdiv(pb.N, gemm_tile_rows()), v_tiles = cdiv(pb.V, kBN);
+  const bool ext = mode == FIN_LOSS && opt_ext_forward(opt);
+  // Valid rows only (the plain epilogue; an ignored row's loss is 0 and its lse is not
+  // needed): the GEMM reads the gathered valid rows of X, with room in the workspace.
+  const FwdCompactLayout C = fwd_compact_layout(pb.N, pb.D, pb.V);
+  const bool compact = FLCE_COMPACT_ROWS && mode == FIN_LOSS && !ext && ws_bytes >= C.total;
 
   // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;
@@ -473,15 +497,24 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
       pb.w_vd ? encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.D), uint64_t(pb.V), uint64_t(pb.D), 64,
                           uint32_t(gemm_b_rows_per_cta()))
               : encode_2d(&tmW, pb.dt16(), 2, pb.W, uint64_t(pb.V), uint64_t(pb.D), uint64_t(pb.V), 64, 64);
+  const void* Xa = compact ? static_cast<const void*>(ws + C.xc) : pb.X;
   const bool enc_x =
-      encode_2d(&tmX, pb.dt16(), 2, pb.X, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64, kBM);
+      encode_2d(&tmX, pb.dt16(), 2, Xa, uint64_t(pb.D), uint64_t(pb.N), uint64_t(pb.D), 64, kBM);
   if (!enc_w || !enc_x) return FLCE_ERR_CUDA;
 
   if (clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(ws, 0, kHeaderBytes, stream));
   const float* cw = opt ? opt->class_weight : nullptr;
   if (cw) FLCE_CUDA_CHECK(launch_sum(cw, int(pb.V), wtot, stream));
-  const bool ext = mode == FIN_LOSS && opt_ext_forward(opt);
   const bool want_idx = ext && (opt->predicted || opt->accuracy);
+  int* n_valid = reinterpret_cast<int*>(ws + kHdrNValid);
+  int* rows = reinterpret_cast<int*>(ws + C.rows);
+  int* slot = reinterpret_cast<int*>(ws + C.slot);
+  if (compact) {
+    const CompactParams cp{pb.targets, int(pb.N), pb.ignore_index, rows, slot, n_valid};
+    FLCE_CUDA_CHECK(launch_compact_rows(cp, stream));
+    const GatherParams gp{pb.X, ws + C.xc, nullptr, nullptr, rows, n_valid, int(pb.N), int(pb.D)};
+    FLCE_CUDA_CHECK(launch_gather_rows(gp, sms, stream));
+  }
 
   FwdParams p{};
   p.targets = pb.targets;
@@ -491,6 +524,8 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   p.v_tiles = int(v_tiles);
   pick_forward_schedule(n_tiles, v_tiles, &p);
   p.ticket = reinterpret_cast<int*>(ws + kHdrTicket);  // zeroed with the header above
+  p.dyn_rows = compact ? n_valid : nullptr;
+  p.row_of = compact ? rows : nullptr;
   if (!clear_header) FLCE_CUDA_CHECK(cudaMemsetAsync(p.ticket, 0, sizeof(int), stream));
   p.num_kb = int(cdiv(pb.D, kBK));
   p.want_sum_z = (mode == FIN_SHARD_STATS) || pb.eps != 0.f;
@@ -529,6 +564,7 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   f.cw = ext ? cw : nullptr;
   f.wtot = wtot;
   f.lse = lse;
+  f.slot = compact ? slot : nullptr;
   f.loss = loss;
   f.stats_out = stats;
   // The argmax decision is made per row in the finalize; without a caller array it
@@ -728,6 +764,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         ww.total_tiles = int(vt * d_tiles_m);
         ww.tiles_minor = int(d_tiles_m);
         ww.col_major = 1;
+        ww.minor_split = (FLCE_DW_MINOR_SPLIT > 1 && d_tiles_m % FLCE_DW_MINOR_SPLIT == 0) ? FLCE_DW_MINOR_SPLIT : 1;
         sw.x_off = int(v0);
         FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, false, pb.f16, stream));
       } else {
@@ -807,8 +844,8 @@ flce_status flce_forward_ex(const void* X, const void* W, const int32_t* targets
     note_error("forward_max_units", "no resident cluster");
     return FLCE_ERR_CUDA;
   }
-  return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), true,
-                     reinterpret_cast<cudaStream_t>(stream));
+  return run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, static_cast<uint8_t*>(workspace), ws_bytes, true,
+                     sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 flce_status flce_forward(const void* X, const void* W, const int32_t* targets, int64_t N, int64_t D, int64_t V,
@@ -877,7 +914,7 @@ flce_status flce_forward_backward(const void* X, const void* W, const int32_t* t
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, true, s)) != FLCE_OK) return st;
+  if ((st = run_forward(pb, opt, FIN_LOSS, 0, loss, lse, nullptr, ws, ws_bytes, true, sms, s)) != FLCE_OK) return st;
   return run_backward(pb, opt, lse, grad_out, dX, dW, ws, false, sms, s);
 }
 
@@ -918,7 +955,7 @@ flce_status flce_shard_stats_ex(const void* X, const void* W, const int32_t* tar
   }
   const Problem pb{X, W, targets, N, D, V, ignore_index, 0.f, 0.f, FLCE_REDUCTION_SUM, opt_w_vd(opt), opt_f16(opt)};
   return run_forward(pb, nullptr, FIN_SHARD_STATS, v_offset, nullptr, nullptr, stats,
-                     static_cast<uint8_t*>(workspace), true, reinterpret_cast<cudaStream_t>(stream));
+                     static_cast<uint8_t*>(workspace), ws_bytes, true, sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 flce_status flce_combine_shards(const float* stats, int32_t K, const int32_t* targets, int64_t N, int64_t v_total,

@@ -178,6 +178,15 @@ struct FwdSched {
       : n_tiles(a.p->n_tiles), v_tiles(a.p->v_tiles), n_blocks(a.p->n_blocks), panel(a.p->panel),
         chunk_tiles(a.p->chunk_tiles), n_chunks(a.p->n_chunks), total_units(a.p->total_units),
         num_kb(a.p->num_kb), ticket(a.p->ticket), ring(a.ring), w(a.w), role(a.role) {
+    if (a.p->dyn_rows != nullptr) {
+      // valid-row compaction: the rows of X are the gathered valid rows; every role reads
+      // the same count, so all of them walk the same units
+      const int n = *a.p->dyn_rows;
+      n_tiles = (n + Geo<CG>::kTileRows - 1) / Geo<CG>::kTileRows;
+      n_blocks = (n_tiles + MC * kFwdRowBlock - 1) / (MC * kFwdRowBlock);
+      total_units = n_blocks * n_chunks;
+    }
+    if (panel > n_blocks) panel = n_blocks;
     const Pair pr = pair_id<CG, MC>();
     rank = pr.rank;
     pair = pr.pair;
@@ -311,8 +320,18 @@ struct WalkSched {
 
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;
-    const int major = i / w.tiles_minor;
-    const int minor = i - major * w.tiles_minor;
+    int major, minor;
+    if (w.minor_split > 1) {
+      const int m = w.tiles_minor / w.minor_split;  // minor tiles per part
+      const int per_part = (w.total_tiles / w.tiles_minor) * m;
+      const int part = i / per_part;
+      const int r = i - part * per_part;
+      major = r / m;
+      minor = part * m + (r - major * m);
+    } else {
+      major = i / w.tiles_minor;
+      minor = i - major * w.tiles_minor;
+    }
     const int rows = (w.col_major ? minor : major) * MC + pair;
     const int cols = w.col_major ? major : minor;
     t.a_row = rows * Geo<CG>::kTileRows + rank * kBM;
@@ -838,6 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ys[q] = -1;
     }
     const bool want_sum = p.want_sum_z != 0;
+    const int n_rows = p.dyn_rows != nullptr ? *p.dyn_rows : p.N;  // rows of X this launch covers
     while (sched.next(t)) {
       if (!epi_acquire(s, acc, acc_phase, epi_tid, w)) break;
       // the statistics of this tile's row tile (register select, no local memory)
@@ -853,8 +873,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t.flags & TILE_FIRST) {
         row = t.a_row + r;
         y = -1;
-        if (row < p.N) {
-          const int yt = __ldg(p.targets + row);
+        if (row < n_rows) {
+          const int yt = __ldg(p.targets + (p.row_of != nullptr ? __ldg(p.row_of + row) : row));
           y = (yt == p.ignore_index) ? -1 : yt - p.y_offset;
         }
         st = Stats{};
@@ -888,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if ((t.flags & TILE_LAST) && row < p.N) {
+      if ((t.flags & TILE_LAST) && row < n_rows) {
         const size_t o = size_t(t.aux) * size_t(p.N) + size_t(row);
         p.part_m[o] = st.m;
         p.part_d[o] = st.d;

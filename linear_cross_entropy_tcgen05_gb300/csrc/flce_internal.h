@@ -56,6 +56,11 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_PAIRS_PER_CLUSTER
 #define FLCE_PAIRS_PER_CLUSTER 2
 #endif
+// dW GEMM of a [D, V] dW: walk the D row groups in this many parts, each part across all
+// vocabulary tiles of the band before the next, so a wave re-reads fewer columns of X.
+#ifndef FLCE_DW_MINOR_SPLIT
+#define FLCE_DW_MINOR_SPLIT 2
+#endif
 // L2 policies (0 normal, 1 evict-first, 2 evict-last) of the dX GEMM's A operand (the
 // gradient band), the dW GEMM's operands, and the gradient GEMM's band store.
 #ifndef FLCE_DX_A_POL
@@ -97,6 +102,8 @@ struct WalkParams {
                      // column in flight), 0: over row-tile groups
   int dyn_mode;          // DynRows: how *dyn_rows bounds the walk (at least one group or block)
   const int* dyn_rows;   // device count of valid rows, or null
+  int minor_split;       // > 1: walk the minor tiles in this many parts, each part across all
+                         // majors before the next (tiles_minor divisible by it); 0 or 1: off
 };
 
 // Rows past the valid-row count that the compacted operands hold as zeros (with an
@@ -116,7 +123,7 @@ struct CompactParams {
 struct GatherParams {
   const void* X;         // 16-bit [N, D]
   void* Xc;              // 16-bit [N, D]: valid rows first, then zeros up to the padding
-  const float4* coef;    // [N] per-row gradient coefficients
+  const float4* coef;    // [N] per-row gradient coefficients, or null (the forward: none)
   float4* coef_c;        // [N] the same in compacted order, ignored-row values in the padding
   const int* rows;
   const int* n_valid;
@@ -140,11 +147,14 @@ struct FwdParams {
   int N, V;
   int n_tiles, v_tiles;
   int n_blocks;     // cluster row blocks (MC pairs x kFwdRowBlock row tiles each)
-  int panel;        // cluster row blocks per panel
+  int panel;        // cluster row blocks per panel (at most; fewer if there are fewer blocks)
   int chunk_tiles;  // vocabulary tiles per chunk; one partial statistic per row and chunk
   int n_chunks;     // chunks over the vocabulary (at most kMaxSplits)
   int total_units;  // n_blocks x n_chunks units, handed out in order by a ticket counter
   int* ticket;      // the counter (zero when the launch starts)
+  const int* dyn_rows;  // valid-row compaction: device count of the rows of X (the valid
+                        // rows, gathered), which replaces N, n_tiles, n_blocks, total_units
+  const int* row_of;    // valid-row compaction: original row of each compacted row, or null
   int num_kb;       // K blocks over D
   int want_sum_z;  // label smoothing needs sum_j z_ij
   int ignore_index;
@@ -208,6 +218,8 @@ struct FinalizeParams {
   const float* cw;      // [V] class weights or null
   const float* wtot;    // device scalar sum_j w_j (with cw)
   float* lse;
+  const int* slot;      // valid-row compaction of the forward: the partial statistics of row r
+                        // sit at slot[r] (-1: an ignored row), or null (at r)
   float* loss;          // [1] or [N]
   float* stats_out;     // FIN_SHARD_STATS: [4][N]
   int* predicted;       // [N] or null

@@ -50,13 +50,16 @@ __global__ void __launch_bounds__(kFinalizeThreads)
         zy += st[2 * size_t(p.N) + row];
         owners += st[3 * size_t(p.N) + row] != 0.f ? 1 : 0;
       }
+    } else if (p.slot != nullptr && p.slot[row] < 0) {
+      // an ignored row of a forward that ran on the valid rows only: no statistics
     } else {
+      const int prow = p.slot != nullptr ? p.slot[row] : row;  // where this row's partials sit
       float best = -CUDART_INF_F;
       for (int s = 0; s < p.S; ++s) {
-        const float m = p.part_m[size_t(s) * p.N + row];
+        const float m = p.part_m[size_t(s) * p.N + prow];
         M = fmaxf(M, m);
         if (p.part_idx != nullptr) {
-          const int idx = p.part_idx[size_t(s) * p.N + row];
+          const int idx = p.part_idx[size_t(s) * p.N + prow];
           if (m > best || (m == best && idx < best_idx)) {
             best = m;
             best_idx = idx;
@@ -64,14 +67,17 @@ __global__ void __launch_bounds__(kFinalizeThreads)
         }
       }
       for (int s = 0; s < p.S; ++s) {
-        const size_t o = size_t(s) * p.N + row;
+        const size_t o = size_t(s) * p.N + prow;
         d += p.part_d[o] * exp2f((p.part_m[o] - M) * kLog2e);
         sz += p.part_s[o];
       }
-      zy = p.tgt[row];
+      zy = p.tgt[prow];
     }
-    const float lse = timed_out ? CUDART_NAN_F : M + logf(d);
     const int y = p.targets[row];
+    // the lse of an ignored row is 0 (the loss needs none; a forward that runs on the
+    // valid rows only does not compute it)
+    float lse = y == p.ignore_index && p.mode != FIN_SHARD_STATS ? 0.f : M + logf(d);
+    if (timed_out) lse = CUDART_NAN_F;
     if (p.mode == FIN_SHARD_STATS) {
       const int rel = y - p.v_offset;
       const bool own = y != p.ignore_index && rel >= 0 && rel < p.V_local;
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(256) flce_gather_rows_kernel(const GatherParam
     const uint4* from = reinterpret_cast<const uint4*>(p.X) + size_t(src) * size_t(n16);
     uint4* to = reinterpret_cast<uint4*>(p.Xc) + size_t(i) * size_t(n16);
     for (int c = lane; c < n16; c += 32) to[c] = valid ? from[c] : make_uint4(0u, 0u, 0u, 0u);
-    if (lane == 0)
+    if (lane == 0 && p.coef_c != nullptr)
       p.coef_c[i] = valid ? p.coef[src] : make_float4(0.f, -CUDART_INF_F, 0.f, __int_as_float(kIgnoredRow));
   }
 }

@@ -75,6 +75,12 @@ def test_workspace_sizes(lib):
     for (n, d, v) in [(256, 128, 1024), (4096, 2048, 32000), (8192, 4096, 128256), (16384, 2304, 256000)]:
         band = flce.flce_workspace_size(n, d, v, True) - n * d * 4 - n * 16 - 256
         assert band < n * v * 2
+        # the forward on the valid rows only: its own workspace plus the row list and the
+        # gathered rows of X; every backward workspace has that room
+        f, fc = flce.flce_workspace_size(n, d, v, "forward"), flce.flce_workspace_size(n, d, v, "forward_valid_rows")
+        assert fc >= f + n * d * 2 + 2 * n * 4
+        assert flce.flce_workspace_size(n, d, v, "backward") >= fc
+        assert flce.flce_workspace_size(n, d, v, "both") >= fc
 
 
 def test_logit_bottleneck_arithmetic():

@@ -53,13 +53,15 @@ def test_bench_makes_no_process_group():
 
 def test_launch_count_matches_the_band_schedule():
     import bench
+    # forward: valid-row list + gather + GEMM + finalize + loss reduction
     total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean")
-    assert (bands, vc) == (21, 6144) and total == 3 + 4 + 3 * 21 + 1   # the workspace's capacity
+    assert (bands, vc) == (21, 6144) and total == 5 + 4 + 3 * 21 + 1   # the workspace's capacity
     total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608)
-    assert bands == 28 and total == 3 + 4 + 3 * 28 + 1                  # a narrower band chosen on the device
-    total, _, _ = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608, compact=False)
+    assert bands == 28 and total == 5 + 4 + 3 * 28 + 1                  # a narrower band chosen on the device
+    total, _, _ = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", 4608, compact=False, compact_fwd=False)
     assert total == 3 + 2 + 3 * 28 + 1                                  # no valid-row compaction
-    total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", row_band=16384)
+    total, bands, vc = bench.kernel_launches_per_step(65536, 4096, 128256, "mean", row_band=16384,
+                                                      compact_fwd=False)
     assert (bands, vc) == (8, 16384) and total == 3 + 1 + 4 * (1 + 2 + 3 * 8 + 1)   # four row bands
 
 

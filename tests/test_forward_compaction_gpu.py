@@ -1,0 +1,84 @@
+"""The forward on the valid rows only. With a workspace of flce_workspace_size(..., 3)
+bytes (every backward workspace has that room) the forward gathers the valid rows of X
+and runs its GEMM on them alone; with the forward's own, smaller workspace it runs on every
+row. The results must be the same bit for bit (each valid row's logits are the same dot
+products in the same order), the lse of an ignored row is exactly 0 either way, and both
+agree with the fp64 oracle on the valid rows."""
+import numpy as np
+import pytest
+import torch
+
+import linear_cross_entropy_tcgen05_gb300 as flce
+import oracle
+from tests.flce_cases import TOL_LOSS_REL, TOL_LSE_ABS
+from workloads import custom, make_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _forward(X, W, y, wl, kind, reduction=None):
+    red = wl.reduction if reduction is None else reduction
+    N, D, V = wl.N, wl.D, wl.V
+    ws = torch.empty(flce.flce_workspace_size(N, D, V, kind), dtype=torch.uint8, device=DEV)
+    loss = torch.full((N if red == "none" else 1,), float("nan"), device=DEV)
+    lse = torch.full((N,), float("nan"), device=DEV)
+    flce.flce_forward(X, W, y, loss, lse, ws, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, red)
+    assert flce.flce_check_device_error(ws) == 0
+    return loss, lse
+
+
+CASES = [
+    custom("fc1", 1000, 136, 4104, seed=301, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-4),
+    custom("fc2", 2048, 256, 8200, seed=302, ignore_frac=0.9, reduction="sum"),
+    custom("fc3", 777, 64, 1000, seed=303, ignore_frac=0.5),
+    custom("fc4", 513, 128, 2048, seed=304, ignore_frac=0.3, reduction="none"),
+]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[c.name for c in CASES])
+def test_valid_rows_forward_is_bitwise_the_full_forward(gpu_lib, wl):
+    X, W, y = make_inputs(wl)
+    Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
+    full = _forward(Xd, Wd, yd, wl, "forward")
+    valid_only = _forward(Xd, Wd, yd, wl, "forward_valid_rows")
+    torch.cuda.synchronize()
+    for a, b in zip(full, valid_only):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ign = (y == wl.ignore_index).numpy()
+    lse = valid_only[1].cpu().double().numpy()
+    assert np.all(lse[ign] == 0.0)
+    ref_loss, ref_lse = oracle.forward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    assert np.max(np.abs(lse[~ign] - ref_lse[~ign])) <= TOL_LSE_ABS
+    got = valid_only[0].cpu().double().numpy()
+    ref = np.atleast_1d(np.asarray(ref_loss, dtype=np.float64))
+    scale = np.maximum(np.abs(ref), 1.0) if wl.reduction == "none" else np.abs(ref)
+    assert np.all(np.abs(got - ref) <= TOL_LOSS_REL * scale)
+
+
+def test_valid_rows_forward_with_every_row_ignored(gpu_lib):
+    wl = custom("fc_all", 700, 64, 1024, seed=305, ignore_frac=1.0)
+    X, W, y = make_inputs(wl)
+    for kind in ("forward", "forward_valid_rows"):
+        loss, lse = _forward(X.to(DEV), W.to(DEV), y.to(DEV), wl, kind)
+        torch.cuda.synchronize()
+        assert loss.item() == 0.0 and torch.all(lse == 0.0)
+
+
+def test_valid_rows_forward_then_backward_matches_the_oracle(gpu_lib):
+    """The backward takes the lse the valid-row forward wrote (0 on ignored rows, which
+    the backward never reads) and gives the oracle's gradients."""
+    from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, CudaRun, rel_fro
+    wl = custom("fc_bwd", 1500, 200, 3000, seed=306, ignore_frac=0.6, label_smoothing=0.1, zloss_scale=1e-3)
+    X, W, y = make_inputs(wl)
+    run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
+    assert run.ws.numel() >= flce.flce_workspace_size(wl.N, wl.D, wl.V, "forward_valid_rows")
+    assert run.forward() == 0 and run.backward() == 0
+    got = run.host()
+    loss, lse, dX, dW = oracle.forward_backward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale,
+                                                wl.reduction)
+    valid = y.numpy() != wl.ignore_index
+    assert abs(got["loss"][0] - loss) <= TOL_LOSS_REL * abs(loss)
+    assert np.max(np.abs(got["lse"][valid] - lse[valid])) <= TOL_LSE_ABS
+    assert np.all(got["lse"][~valid] == 0.0)
+    assert rel_fro(got["dX"], dX) <= TOL_DX_REL and rel_fro(got["dW"], dW) <= TOL_DW_REL

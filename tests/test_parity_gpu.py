@@ -157,7 +157,8 @@ def test_autograd_wrapper(gpu_lib):
 
 
 def test_zero_weights_give_the_closed_form(gpu_lib):
-    """W = 0: every logit is 0, lse = ln V, loss = ln V + s (ln V)^2, dX = 0 and
+    """W = 0: every logit is 0, lse = ln V (0 on an ignored row, whose lse the forward
+    does not compute), loss = ln V + s (ln V)^2, dX = 0 and
     dZ = g (p (1 + 2 s lse) - (1 - eps) onehot - eps/V) with p = 1/V (the oracle's own pin,
     here on the GPU)."""
     import math
@@ -170,7 +171,8 @@ def test_zero_weights_give_the_closed_form(gpu_lib):
     got = run.host()
     lnV = math.log(wl.V)
     valid = y.numpy() != wl.ignore_index
-    assert np.max(np.abs(got["lse"] - lnV)) <= 1e-5
+    assert np.max(np.abs(got["lse"][valid] - lnV)) <= 1e-5
+    assert np.all(got["lse"][~valid] == 0.0)
     assert abs(got["loss"][0] - (lnV + 1e-3 * lnV * lnV)) <= 1e-5
     assert np.all(got["dX"] == 0.0)
     _, _, _, ref_dW = oracle.forward_backward(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, "mean")

@@ -555,7 +555,7 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
     sustained = float(peaks.get("bf16_tflops_sustained", burst))
     launches, bands, vc = kernel_launches_per_step(N, D, V, wl.reduction, band_width,
                                                    row_band=args.row_band if 0 < args.row_band < N else 0,
-                                                   compact_fwd=max(ws_f, ws_b) >= ws_fc)
+                                                   compact_fwd=max(ws_f, ws_b) >= ws_fc and N >= 2048)
     cpu = None
     if not args.no_cpu_baseline:
         rate, rows, dt = oracle_sample_for(wl, X, W, y, args.cpu_seconds)

@@ -107,7 +107,7 @@ typedef enum {
  * band of N x Vc columns (Vc a multiple of 512, at most 16384, and below V once V
  * exceeds 512) and an fp32 [N, D] dX accumulator; no buffer has N x V elements.
  * for_backward == 3 gives the size from which flce_forward (without the argmax and
- * epilogue options) runs its GEMM on the valid rows only, gathered into the workspace:
+ * epilogue options, N >= 2048) runs its GEMM on the valid rows only, gathered into the workspace:
  * the forward's own size plus the row list and the valid rows of X (N x D 16-bit values).
  * Any backward or fused workspace has that room. The results are the same either way,
  * bit for bit; only the time differs. */
@@ -268,9 +268,10 @@ flce_status flce_check_device_error(void* workspace, struct CUstream_st* stream)
 /* A static, human-readable name for a status. */
 const char* flce_status_string(flce_status status);
 
-/* Library version as MAJOR*10000 + MINOR*100 + PATCH: 200 (0.2.0). 0.2 grew flce_options
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH: 300 (0.3.0). 0.2 grew flce_options
  * (weight_layout, input_dtype, accumulate_grads at its end): code built against 0.1's
- * header must be rebuilt. */
+ * header must be rebuilt. 0.3: the forward writes lse 0 for ignored rows (it may skip
+ * them), and flce_workspace_size takes for_backward == 3. */
 int flce_version(void);
 
 /* Which call failed the last time an entry point returned FLCE_ERR_CUDA on the calling

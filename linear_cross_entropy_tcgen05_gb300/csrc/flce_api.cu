@@ -378,7 +378,7 @@ void pick_forward_schedule(int64_t n_tiles, int64_t v_tiles, FwdParams* p) {
 
 extern "C" {
 
-int flce_version(void) { return 200; }
+int flce_version(void) { return 300; }
 
 const char* flce_last_error_detail(void) { return g_detail; }
 
@@ -489,7 +489,8 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   // Valid rows only (the plain epilogue; an ignored row's loss is 0 and its lse is not
   // needed): the GEMM reads the gathered valid rows of X, with room in the workspace.
   const FwdCompactLayout C = fwd_compact_layout(pb.N, pb.D, pb.V);
-  const bool compact = FLCE_COMPACT_ROWS && mode == FIN_LOSS && !ext && ws_bytes >= C.total;
+  // (from 2048 rows: below that the two extra launches cost more than the rows they save)
+  const bool compact = FLCE_COMPACT_ROWS && mode == FIN_LOSS && !ext && ws_bytes >= C.total && pb.N >= 2048;
 
   // B = W: MN-major 64 x 64 boxes of W [D, V], or K-major boxes of W [V, D]
   CUtensorMap tmX, tmW;

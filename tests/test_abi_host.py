@@ -53,7 +53,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert flce.flce_version() == 200
+    assert flce.flce_version() == 300
     for code, name in flce.STATUS.items():
         assert flce.flce_status_string(code).startswith(name)
     assert "unknown" in flce.flce_status_string(99)

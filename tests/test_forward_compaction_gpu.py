@@ -1,7 +1,8 @@
 """The forward on the valid rows only. With a workspace of flce_workspace_size(..., 3)
 bytes (every backward workspace has that room) the forward gathers the valid rows of X
 and runs its GEMM on them alone; with the forward's own, smaller workspace it runs on every
-row. The results must be the same bit for bit (each valid row's logits are the same dot
+row (the valid-row path needs 2048 rows or more, so every case here has them). The
+results must be the same bit for bit (each valid row's logits are the same dot
 products in the same order), the lse of an ignored row is exactly 0 either way, and both
 agree with the fp64 oracle on the valid rows."""
 import numpy as np
@@ -29,15 +30,16 @@ def _forward(X, W, y, wl, kind, reduction=None):
 
 
 CASES = [
-    custom("fc1", 1000, 136, 4104, seed=301, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-4),
+    custom("fc1", 2100, 136, 4104, seed=301, ignore_frac=0.1, label_smoothing=0.1, zloss_scale=1e-4),
     custom("fc2", 2048, 256, 8200, seed=302, ignore_frac=0.9, reduction="sum"),
-    custom("fc3", 777, 64, 1000, seed=303, ignore_frac=0.5),
-    custom("fc4", 513, 128, 2048, seed=304, ignore_frac=0.3, reduction="none"),
+    custom("fc3", 2777, 64, 1000, seed=303, ignore_frac=0.5),
+    custom("fc4", 2561, 128, 2048, seed=304, ignore_frac=0.3, reduction="none"),
 ]
 
 
 @pytest.mark.parametrize("wl", CASES, ids=[c.name for c in CASES])
 def test_valid_rows_forward_is_bitwise_the_full_forward(gpu_lib, wl):
+    assert wl.N >= 2048
     X, W, y = make_inputs(wl)
     Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
     full = _forward(Xd, Wd, yd, wl, "forward")
@@ -57,7 +59,7 @@ def test_valid_rows_forward_is_bitwise_the_full_forward(gpu_lib, wl):
 
 
 def test_valid_rows_forward_with_every_row_ignored(gpu_lib):
-    wl = custom("fc_all", 700, 64, 1024, seed=305, ignore_frac=1.0)
+    wl = custom("fc_all", 2100, 64, 1024, seed=305, ignore_frac=1.0)
     X, W, y = make_inputs(wl)
     for kind in ("forward", "forward_valid_rows"):
         loss, lse = _forward(X.to(DEV), W.to(DEV), y.to(DEV), wl, kind)
@@ -69,7 +71,7 @@ def test_valid_rows_forward_then_backward_matches_the_oracle(gpu_lib):
     """The backward takes the lse the valid-row forward wrote (0 on ignored rows, which
     the backward never reads) and gives the oracle's gradients."""
     from tests.flce_cases import TOL_DW_REL, TOL_DX_REL, CudaRun, rel_fro
-    wl = custom("fc_bwd", 1500, 200, 3000, seed=306, ignore_frac=0.6, label_smoothing=0.1, zloss_scale=1e-3)
+    wl = custom("fc_bwd", 2500, 200, 3000, seed=306, ignore_frac=0.6, label_smoothing=0.1, zloss_scale=1e-3)
     X, W, y = make_inputs(wl)
     run = CudaRun(X, W, y, wl.ignore_index, wl.label_smoothing, wl.zloss_scale, wl.reduction)
     assert run.ws.numel() >= flce.flce_workspace_size(wl.N, wl.D, wl.V, "forward_valid_rows")

@@ -382,6 +382,7 @@ def run_ours(args, wl):
     ms_step = total_ms / args.steps
     value = N / (ms_step / 1000.0)
     band_width = flce.flce_backward_band_width(N, D, V, pb.opt_b) or None
+    kernels = profile_gemm_kinds(pb, args.profile_steps)
 
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
     e2e_value, e2e_ms, h2d, d2h = run_e2e(args, dev, stream, X, W, y, pb)
@@ -390,10 +391,62 @@ def run_ours(args, wl):
     torch.cuda.empty_cache()
     side = run_side_workloads(args, flce, dev, stream) if args.side_workloads else None
     return finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes,
-                  e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width, side,
+                  e2e_value, e2e_ms, h2d, d2h, clk, launches_timed, band_width, side, kernels,
                   flce.flce_workspace_size(N, D, V, False),
                   flce.flce_workspace_size(args.row_band if 0 < args.row_band < N else N, D, V, True),
                   flce.flce_workspace_size(N, D, V, "forward_valid_rows"))
+
+
+def profile_gemm_kinds(pb, steps):
+    """Device time of each GEMM kind per step, measured live: `steps` more forward +
+    backward steps after the timed region with the library's launch events on
+    (flce_profile_gemms: a CUDA event pair on the call's stream around every GEMM
+    launch). Returns {kind: {"ms_per_step", "launches_per_step", "avg_launch_ms"}} and
+    the profiled steps' own time per step."""
+    flce = pb.flce
+    if steps <= 0:
+        return None
+    torch.cuda.synchronize(pb.dev)
+    flce.flce_profile_read()  # nothing pending
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flce.flce_profile_gemms(True)
+    try:
+        start.record(pb.stream)
+        for _ in range(steps):
+            pb.fwd()
+            pb.bwd()
+        end.record(pb.stream)
+        torch.cuda.synchronize(pb.dev)
+    finally:
+        flce.flce_profile_gemms(False)
+    pb.check("in the profiled steps")
+    out = {}
+    for kind, (ms, n) in flce.flce_profile_read().items():
+        if n:
+            out[kind] = {"ms_per_step": ms / steps, "launches_per_step": n / steps, "avg_launch_ms": ms / n}
+    return {"kinds": out, "step_ms": start.elapsed_time(end) / steps, "steps": steps}
+
+
+KERNEL_NAMES = {"forward": "flce_forward_gemm_kernel (forward GEMM + online softmax)",
+                "gradient": "flce_walk_gemm_kernel (gradient GEMM: recomputed logits -> G band)",
+                "dW": "flce_walk_gemm_kernel (dW GEMM: X^T G, K = valid rows)",
+                "dX": "flce_walk_gemm_kernel (dX GEMM: G W^T, fp32 accumulate)"}
+
+
+def recorded_traffic(kind):
+    """A one-pass ncu capture of this GEMM kind's DRAM bytes per launch at the headline
+    shape, recorded under profiles/ with the hash of the kernel source it was taken on;
+    None unless that hash matches the source."""
+    p = os.path.join(ROOT, "profiles", "gemm_traffic_headline.json")
+    if not os.path.exists(p):
+        return None, None
+    rec = json.load(open(p))
+    if rec.get("kernel_source_hash") != _kernel_hash() or kind not in rec.get("kinds", {}):
+        return None, None
+    k = rec["kinds"][kind]
+    return k["bytes_per_launch"], {"kind": "recorded ncu capture of this kernel source, not measured in this run",
+                                   "captured": rec.get("captured"), "case": k.get("launch"),
+                                   "record": "profiles/gemm_traffic_headline.json"}
 
 
 def run_e2e(args, dev, stream, X, W, y, pb):
@@ -544,7 +597,7 @@ def run_side_workloads(args, flce, dev, stream):
 
 
 def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_alloc, extra_bytes, e2e_value, e2e_ms,
-           h2d, d2h, clk, launches_timed, band_width, side, ws_f, ws_b, ws_fc):
+           h2d, d2h, clk, launches_timed, band_width, side, kernels, ws_f, ws_b, ws_fc):
     peaks, peak_kind = measured_peaks()
     flops_step = 8.0 * N * D * V
     fwd_avg = statistics.mean(fwd_ms)
@@ -562,15 +615,39 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"fp64 oracle fwd+bwd of the first {rows} rows x full V in chunks of 256 "
                          f"({dt:.1f} s); tokens/s = rows/time"}
-    traffic, traffic_source = None, None
-    tr_path = os.path.join(ROOT, "profiles", "forward_gemm_traffic.json")
-    if os.path.exists(tr_path):
-        tr = json.load(open(tr_path))
-        if tr.get("kernel_source_hash") == _kernel_hash():
-            traffic = tr.get("bytes_per_launch")
-            traffic_source = {"kind": "recorded ncu capture of this kernel source, not measured in this run",
-                              "captured": tr.get("captured"), "case": tr.get("captured_case"),
-                              "record": "profiles/forward_gemm_traffic.json"}
+    # every GEMM kind does 2*N*D*V algorithmic flops per step (all rows, as counted for the
+    # step), spread over its launches; the roofline object is the kind with the most time
+    valid_rows = int((y != wl.ignore_index).sum())
+    per_kind = {}
+    dominant = None
+    if kernels:
+        for kind, k in kernels["kinds"].items():
+            tf = 2.0 * N * D * V / (k["ms_per_step"] / 1000.0) / 1e12
+            traffic, source = recorded_traffic(kind)
+            per_kind[kind] = {"kernel": KERNEL_NAMES.get(kind, kind), "ms_per_step": k["ms_per_step"],
+                              "launches_per_step": k["launches_per_step"], "avg_launch_ms": k["avg_launch_ms"],
+                              "achieved": tf, "frac": tf / sustained,
+                              "achieved_valid_rows": tf * valid_rows / N,
+                              "traffic": traffic, "traffic_source": source}
+        dominant = max(per_kind, key=lambda kd: per_kind[kd]["ms_per_step"])
+    if dominant is not None:
+        dk = per_kind[dominant]
+        roofline = {"kernel": dk["kernel"], "bound": "tensor", "achieved": dk["achieved"], "peak": sustained,
+                    "unit": "TFLOP/s", "frac": dk["frac"], "traffic": dk["traffic"],
+                    "traffic_source": dk["traffic_source"],
+                    "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (kernels timed inside a seconds-long loop)",
+                    "frac_of_burst": dk["achieved"] / burst,
+                    "algorithmic": "2*N*D*V flops per step over the kind's launches (all rows counted)",
+                    "avg_launch_ms": dk["avg_launch_ms"], "launches_per_step": dk["launches_per_step"],
+                    "share_of_gemm_time": dk["ms_per_step"] / sum(v["ms_per_step"] for v in per_kind.values()),
+                    "frac_valid_rows": dk["achieved_valid_rows"] / sustained,
+                    "measured": (f"CUDA events around every launch of the kind on its stream "
+                                 f"(flce_profile_gemms), {kernels['steps']} steps after the timed region "
+                                 f"({kernels['step_ms']:.2f} ms per profiled step)")}
+    else:
+        roofline = {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
+                    "peak": sustained, "unit": "TFLOP/s", "frac": fwd_gemm_tf / sustained, "traffic": None,
+                    "traffic_source": None}
     liger_b200 = 65536 / 0.194
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
@@ -592,14 +669,13 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
         "peak_mb": {"total": peak_alloc / 2**20, "extra": extra_bytes / 2**20,
                     "workspace": max(ws_f, ws_b) / 2**20,
                     "logits_bf16_would_be": N * V * 2 / 2**20},
-        # the forward is timed inside a seconds-long fwd+bwd loop at the board's power limit,
-        # so its peak is the sustained cuBLAS figure; the burst fraction is given beside it
-        "roofline": {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
-                     "peak": sustained, "unit": "TFLOP/s", "frac": fwd_gemm_tf / sustained, "traffic": traffic,
-                     "traffic_source": traffic_source,
-                     "peak_kind": f"{peak_kind} sustained cuBLAS bf16 (kernel timed inside the step loop)",
-                     "frac_of_burst": fwd_gemm_tf / burst,
-                     "algorithmic": "2*N*D*V flops per launch (forward call = GEMM + finalize)"},
+        # the kernels run inside a seconds-long fwd+bwd loop at the board's power limit, so
+        # their peak is the sustained cuBLAS figure; the burst fraction is given beside it
+        "roofline": roofline,
+        "roofline_kernels": per_kind,
+        "roofline_forward_call": {"achieved": fwd_gemm_tf, "frac": fwd_gemm_tf / sustained, "unit": "TFLOP/s",
+                                  "algorithmic": "2*N*D*V flops over the forward call (GEMM + finalize), "
+                                                 "timed in the timed region"},
         "roofline_step": {"bound": "tensor", "achieved": step_tf, "peak": sustained, "unit": "TFLOP/s",
                           "frac": step_tf / sustained, "peak_kind": f"{peak_kind} sustained cuBLAS bf16",
                           "algorithmic": "8*N*D*V flops per step"},
@@ -654,6 +730,8 @@ def main():
     ap.add_argument("--side-workloads", default=SIDE_DEFAULT,
                     help="comma-separated workloads timed after the main one ('' for none)")
     ap.add_argument("--side-seconds", type=float, default=0.5, help="timed seconds per side workload")
+    ap.add_argument("--profile-steps", type=int, default=3,
+                    help="steps after the timed region with per-GEMM-kind device timing (0: none)")
     ap.add_argument("--wait-stats", action="store_true",
                     help="with --only and a library built with -DFLCE_WAIT_STATS=1: print pipeline wait shares")
     ap.add_argument("--only", choices=["fwd", "bwd"], default=None,

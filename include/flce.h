@@ -289,6 +289,16 @@ const char* flce_last_error_detail(void);
  * For profiling and launch accounting; the pages have no counterpart. */
 unsigned long long flce_kernel_launches(void);
 
+/* Diagnostic device timing of the tensor-core GEMMs. With flce_profile_gemms(1), every
+ * later GEMM launch of any thread is bracketed by two CUDA events recorded on the call's
+ * stream (created per launch; not for use under stream capture); flce_profile_gemms(0)
+ * stops that. flce_profile_read waits for the events recorded so far, adds their elapsed
+ * times and counts per GEMM kind into ms[4] and launches[4] (0 forward, 1 gradient,
+ * 2 dW, 3 dX), releases them, and returns FLCE_OK (FLCE_ERR_CUDA if an event failed).
+ * For measuring each kernel's share of a step live; the pages have no counterpart. */
+void flce_profile_gemms(int enable);
+flce_status flce_profile_read(double* ms, unsigned long long* launches);
+
 /* Width (vocabulary columns) of the gradient bands flce_backward uses for this shape on
  * the current device: a multiple of 512 at most the workspace's band capacity, chosen so
  * that the dW GEMM's launches fill the device's resident clusters evenly. opt may be

@@ -26,7 +26,8 @@ __all__ = [
     "LinearCrossEntropyFunction", "REDUCTIONS", "STATUS", "logits_bytes", "EXPORTED_SYMBOLS", "FlceOptions",
     "make_options", "flce_forward_ex", "flce_backward_ex", "flce_forward_backward", "flce_shard_stats",
     "flce_combine_shards", "WEIGHT_LAYOUTS", "INPUT_DTYPES", "flce_last_error_detail", "flce_kernel_launches",
-    "flce_selftest_wait_timeout", "flce_backward_band_width", "FusedLinearCrossEntropyLoss",
+    "flce_selftest_wait_timeout", "flce_backward_band_width", "FusedLinearCrossEntropyLoss", "flce_profile_gemms",
+    "flce_profile_read", "GEMM_KINDS", "WORKSPACE_KINDS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,7 +45,9 @@ EXPORTED_SYMBOLS = ("flce_workspace_size", "flce_forward", "flce_backward", "flc
                     "flce_status_string", "flce_version", "flce_forward_noalloc", "flce_forward_ex",
                     "flce_backward_ex", "flce_forward_backward", "flce_shard_stats", "flce_combine_shards",
                     "flce_last_error_detail", "flce_shard_stats_ex", "flce_kernel_launches",
-                    "flce_selftest_wait_timeout", "flce_backward_band_width")
+                    "flce_selftest_wait_timeout", "flce_backward_band_width", "flce_profile_gemms",
+                    "flce_profile_read")
+GEMM_KINDS = ("forward", "gradient", "dW", "dX")  # the order of flce_profile_read's arrays
 
 
 class FlceOptions(ctypes.Structure):
@@ -135,6 +138,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.flce_selftest_wait_timeout.restype = ctypes.c_int
     lib.flce_backward_band_width.argtypes = [i64, i64, i64, vp]
     lib.flce_backward_band_width.restype = i64
+    lib.flce_profile_gemms.argtypes = [ctypes.c_int]
+    lib.flce_profile_gemms.restype = None
+    lib.flce_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_ulonglong)]
+    lib.flce_profile_read.restype = ctypes.c_int
     op = ctypes.POINTER(FlceOptions)
     lib.flce_forward_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, f32, f32, ctypes.c_int, op, vp, vp, vp, sz, vp]
     lib.flce_forward_ex.restype = ctypes.c_int
@@ -177,6 +184,20 @@ def flce_backward_band_width(N: int, D: int, V: int, options: FlceOptions | None
 def flce_kernel_launches() -> int:
     """Kernels the library has launched in this process so far."""
     return int(load_library().flce_kernel_launches())
+
+
+def flce_profile_gemms(enable: bool) -> None:
+    """Bracket every later GEMM launch with CUDA events (diagnostics), or stop."""
+    load_library().flce_profile_gemms(1 if enable else 0)
+
+
+def flce_profile_read() -> dict:
+    """{kind: (device ms summed, launches)} of the GEMM launches timed since the last read
+    (kinds as in GEMM_KINDS); waits for their events."""
+    ms = (ctypes.c_double * 4)()
+    n = (ctypes.c_ulonglong * 4)()
+    _check(load_library().flce_profile_read(ms, n), "flce_profile_read")
+    return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(GEMM_KINDS)}
 
 
 def flce_last_error_detail() -> str:

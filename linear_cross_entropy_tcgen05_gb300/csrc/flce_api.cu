@@ -384,6 +384,14 @@ const char* flce_last_error_detail(void) { return g_detail; }
 
 unsigned long long flce_kernel_launches(void) { return launches_so_far(); }
 
+void flce_profile_gemms(int enable) { profile_enable(enable != 0); }
+
+flce_status flce_profile_read(double* ms, unsigned long long* launches) {
+  if (!ms || !launches) return FLCE_ERR_INVALID_ARG;
+  FLCE_CUDA_CHECK(profile_read(ms, launches));
+  return FLCE_OK;
+}
+
 flce_status flce_selftest_wait_timeout(void* workspace, size_t ws_bytes, struct CUstream_st* stream_) {
   if (!workspace) return FLCE_ERR_INVALID_ARG;
   if (!aligned(workspace, 16)) return FLCE_ERR_ALIGNMENT;

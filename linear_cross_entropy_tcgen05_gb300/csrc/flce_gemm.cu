@@ -1208,7 +1208,11 @@ cudaError_t launch_walk(Kern kernel, const CUtensorMap& tmA, const CUtensorMap& 
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_config(clusters * kCG * kMC, kWalkSmem, stream, attr);
   count_launch();
-  return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, w, g, s);
+  const int kind = slot == 1 ? GEMM_GRADIENT : slot == 2 ? GEMM_DW : GEMM_DX;
+  profile_begin(kind, stream);
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, w, g, s);
+  profile_end(kind, stream);
+  return e;
 }
 
 }  // namespace
@@ -1256,7 +1260,10 @@ cudaError_t launch_forward_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, 
   const int clusters = p.total_units < maxc ? p.total_units : maxc;
   cudaLaunchConfig_t cfg = make_config(clusters * kCG * kMC, kFwdSmem, stream, attr);
   count_launch();
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  profile_begin(GEMM_FORWARD, stream);
+  e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  profile_end(GEMM_FORWARD, stream);
+  return e;
 }
 
 cudaError_t launch_grad_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,

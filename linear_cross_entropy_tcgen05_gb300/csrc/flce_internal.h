@@ -319,4 +319,12 @@ constexpr int kFinalizeThreads = 256;
 void count_launch();
 unsigned long long launches_so_far();
 
+// Diagnostic device timing of the GEMM launches (flce_profile_gemms / flce_profile_read):
+// when enabled, every GEMM launch is bracketed by a pair of CUDA events on its stream.
+enum GemmKind : int { GEMM_FORWARD = 0, GEMM_GRADIENT = 1, GEMM_DW = 2, GEMM_DX = 3, GEMM_KINDS = 4 };
+void profile_begin(int kind, cudaStream_t stream);
+void profile_end(int kind, cudaStream_t stream);
+void profile_enable(bool on);
+cudaError_t profile_read(double* ms, unsigned long long* launches);
+
 }  // namespace flce

@@ -4,6 +4,8 @@
 // per-row gradient coefficients), the valid-row compaction of the backward, and the
 // fp32 -> bf16 cast of dX.
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -421,11 +423,76 @@ __global__ void __launch_bounds__(64) flce_wait_selftest_kernel(int* err) {
 // ---------------------------------------------------------------------------------
 namespace {
 std::atomic<unsigned long long> g_launches{0};
+
+// Device timing of the GEMM launches, for diagnostics: event pairs recorded around each
+// launch while enabled, read (and released) by profile_read.
+struct ProfRecord {
+  int kind;
+  cudaEvent_t start, stop;
+};
+std::atomic<bool> g_prof_on{false};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_prof;
+thread_local cudaEvent_t t_prof_start[GEMM_KINDS] = {};
 }  // namespace
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 unsigned long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
+
+void profile_begin(int kind, cudaStream_t stream) {
+  if (!g_prof_on.load(std::memory_order_relaxed) || kind < 0 || kind >= GEMM_KINDS) return;
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess || cudaEventRecord(e, stream) != cudaSuccess) {
+    if (e) cudaEventDestroy(e);
+    cudaGetLastError();
+    return;
+  }
+  t_prof_start[kind] = e;
+}
+
+void profile_end(int kind, cudaStream_t stream) {
+  if (kind < 0 || kind >= GEMM_KINDS || t_prof_start[kind] == nullptr) return;
+  cudaEvent_t start = t_prof_start[kind], stop = nullptr;
+  t_prof_start[kind] = nullptr;
+  if (cudaEventCreate(&stop) != cudaSuccess || cudaEventRecord(stop, stream) != cudaSuccess) {
+    if (stop) cudaEventDestroy(stop);
+    cudaEventDestroy(start);
+    cudaGetLastError();
+    return;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof.push_back(ProfRecord{kind, start, stop});
+}
+
+void profile_enable(bool on) { g_prof_on.store(on, std::memory_order_relaxed); }
+
+cudaError_t profile_read(double* ms, unsigned long long* launches) {
+  std::vector<ProfRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  for (int k = 0; k < GEMM_KINDS; ++k) {
+    ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  cudaError_t first = cudaSuccess;
+  for (const ProfRecord& r : recs) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+    if (e == cudaSuccess) {
+      ms[r.kind] += double(t);
+      launches[r.kind] += 1;
+    } else if (first == cudaSuccess) {
+      first = e;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  return first;
+}
 
 cudaError_t launch_finalize(const FinalizeParams& p, int blocks, cudaStream_t stream) {
   flce_finalize_rows_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(p);

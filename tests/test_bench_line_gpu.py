@@ -30,6 +30,12 @@ def test_bench_line_carries_the_contract(gpu_lib):
     roof = d["roofline"]
     assert roof["bound"] == "tensor" and roof["unit"] == "TFLOP/s" and roof["peak"] > 0
     assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-9
+    # the roofline is the GEMM kind with the most device time, timed live per launch
+    kinds = d["roofline_kernels"]
+    assert set(kinds) == {"forward", "gradient", "dW", "dX"}
+    top = max(kinds, key=lambda k: kinds[k]["ms_per_step"])
+    assert roof["kernel"] == kinds[top]["kernel"] and roof["achieved"] == kinds[top]["achieved"]
+    assert kinds["forward"]["launches_per_step"] == 1 and kinds["dX"]["launches_per_step"] >= 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0

@@ -251,11 +251,13 @@ def test_row_band_backward_matches_the_oracle(gpu_lib, row_band, opts):
     assert st == 4
 
 
-def test_launch_counter_matches_the_band_schedule(gpu_lib):
+@pytest.mark.parametrize("N", [1000, 2500], ids=["forward_all_rows", "forward_valid_rows"])
+def test_launch_counter_matches_the_band_schedule(gpu_lib, N):
     """flce_kernel_launches counts what the bench reports as gpu_launches; one forward
-    plus backward launches what the band schedule predicts."""
+    plus backward launches what the band schedule predicts (from 2048 rows the forward
+    adds its valid-row list and gather)."""
     import bench
-    wl = custom("count", 1000, 136, 4104, seed=37, ignore_frac=0.1)
+    wl = custom("count", N, 136, 4104, seed=37, ignore_frac=0.1)
     X, W, y, _, _ = _inputs(wl)
     N, D, V = wl.N, wl.D, wl.V
     Xd, Wd, yd = X.to(DEV), W.to(DEV), y.to(DEV)
@@ -270,7 +272,8 @@ def test_launch_counter_matches_the_band_schedule(gpu_lib):
     assert flce.flce_check_device_error(ws) == 0
     vc = flce.flce_backward_band_width(N, D, V)
     assert vc > 0 and vc % 512 == 0
-    expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean", vc)
+    assert ws.numel() >= flce.flce_workspace_size(N, D, V, "forward_valid_rows")
+    expected, bands, _ = bench.kernel_launches_per_step(N, D, V, "mean", vc, compact_fwd=N >= 2048)
     assert bands == -(-V // vc) and counted == expected
 
 

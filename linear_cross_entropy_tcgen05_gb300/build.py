@@ -62,6 +62,6 @@ def build(verbose: bool = False, extra: list[str] | None = None) -> str:
 
 if __name__ == "__main__":
     # python -m linear_cross_entropy_tcgen05_gb300.build [-v] [-DNAME=VALUE ...]
-    # -D sets a compile-time tunable of the kernels (e.g. -DFLCE_FWD_GN=1).
+    # -D sets a compile-time tunable of the kernels (e.g. -DFLCE_FWD_PANEL=4).
     defines = [a for a in sys.argv[1:] if a.startswith("-D")]
     print(build(verbose="-v" in sys.argv, extra=defines))

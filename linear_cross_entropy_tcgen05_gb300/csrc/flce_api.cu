@@ -350,7 +350,6 @@ flce_status check_common(const void* X, const void* W, const int32_t* targets, i
   return FLCE_OK;
 }
 
-// Forward grid: gN row blocks x S vocabulary ranges = the resident CTA pairs.
 // The forward's units: cluster row blocks x vocabulary chunks (at most kMaxSplits chunks,
 // so at most that many partial statistics per row), walked panel by panel.
 void pick_forward_schedule(int64_t n_tiles, int64_t v_tiles, FwdParams* p) {

@@ -76,7 +76,7 @@ struct Tile {
   int a_k0;    // K coordinate of the first K block in A
   int b_k0;    // ... and in B
   int num_kb;  // number of 64-wide K blocks
-  int aux;     // forward: vocabulary range index of the partial statistics
+  int aux;     // forward: vocabulary chunk of the partial statistics
   int sub;     // forward: row tile within the row block
   int flags;
 };

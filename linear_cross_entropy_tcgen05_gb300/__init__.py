@@ -405,7 +405,11 @@ class LinearCrossEntropyFunction(torch.autograd.Function):
         with torch.cuda.device(X.device):
             N, D = X.shape
             V = W.shape[0] if layout == 1 else W.shape[1]
-            ws = _workspace(N, D, V, X.device, False)
+            # training: a workspace with room for the valid-row forward (the backward's own
+            # workspace, allocated next, is larger, so the peak does not grow); inference: the
+            # forward's minimum
+            training = bool(ctx.needs_input_grad[0] or ctx.needs_input_grad[1])
+            ws = _workspace(N, D, V, X.device, "forward_valid_rows" if training else False)
             loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=X.device)
             lse = torch.empty(N, dtype=torch.float32, device=X.device)
             b32 = bias.detach().float().contiguous() if bias is not None else None

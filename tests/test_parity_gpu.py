@@ -142,9 +142,11 @@ def test_ignored_rows_do_not_change_dw(gpu_lib):
     assert np.array_equal(a["dW"], b["dW"])
 
 
-def test_autograd_wrapper(gpu_lib):
+@pytest.mark.parametrize("N", [384, 2300], ids=["small", "valid_row_forward"])
+def test_autograd_wrapper(gpu_lib, N):
+    """Through torch.autograd; from 2048 rows a training forward runs on the valid rows."""
     import linear_cross_entropy_tcgen05_gb300 as flce
-    wl = custom("ag", 384, 128, 1024, seed=19, ignore_frac=0.1)
+    wl = custom("ag", N, 128, 1024, seed=19, ignore_frac=0.1)
     X, W, y = make_inputs(wl)
     Xd = X.cuda().requires_grad_(True)
     Wd = W.cuda().requires_grad_(True)

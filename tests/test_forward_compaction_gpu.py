@@ -84,3 +84,51 @@ def test_valid_rows_forward_then_backward_matches_the_oracle(gpu_lib):
     assert np.max(np.abs(got["lse"][valid] - lse[valid])) <= TOL_LSE_ABS
     assert np.all(got["lse"][~valid] == 0.0)
     assert rel_fro(got["dX"], dX) <= TOL_DX_REL and rel_fro(got["dW"], dW) <= TOL_DW_REL
+
+
+def _random_case(i):
+    g = np.random.default_rng(7000 + i)
+    return dict(N=int(g.integers(2048, 5000)), D=8 * int(g.integers(1, 40)), V=8 * int(g.integers(1, 600)),
+                seed=7100 + i, ignore_frac=float(g.choice([0.0, 0.1, 0.5, 0.9])),
+                eps=float(g.choice([0.0, 0.1])), s=float(g.choice([0.0, 1e-3])),
+                red=str(g.choice(["mean", "sum", "none"])), layout=str(g.choice(["dv", "vd"])),
+                dtype=str(g.choice(["bf16", "f16"])))
+
+
+RANDOM = [_random_case(i) for i in range(8)]
+
+
+@pytest.mark.parametrize("c", RANDOM, ids=[f"{c['N']}x{c['D']}x{c['V']}-{c['layout']}-{c['dtype']}-{c['red']}"
+                                           for c in RANDOM])
+def test_valid_rows_forward_random_shapes(gpu_lib, c):
+    """Seeded random shapes and options on the valid-row path (both weight layouts, bf16
+    and f16): bit for bit the all-rows forward, and the oracle on the valid rows."""
+    dt = torch.float16 if c["dtype"] == "f16" else torch.bfloat16
+    wl = custom("fcr", c["N"], c["D"], c["V"], seed=c["seed"], ignore_frac=c["ignore_frac"],
+                label_smoothing=c["eps"], zloss_scale=c["s"], reduction=c["red"])
+    X, W, y = make_inputs(wl, dtype=dt)
+    N, D, V = wl.N, wl.D, wl.V
+    Wdev = (W.t().contiguous() if c["layout"] == "vd" else W).to(DEV)
+    Xd, yd = X.to(DEV), y.to(DEV)
+    opt = flce.make_options(weight_layout=c["layout"], input_dtype=dt)
+    outs = []
+    for kind in ("forward", "forward_valid_rows"):
+        ws = torch.empty(flce.flce_workspace_size(N, D, V, kind), dtype=torch.uint8, device=DEV)
+        loss = torch.full((N if c["red"] == "none" else 1,), float("nan"), device=DEV)
+        lse = torch.full((N,), float("nan"), device=DEV)
+        flce.flce_forward_ex(Xd, Wdev, yd, loss, lse, ws, wl.ignore_index, c["eps"], c["s"], c["red"], options=opt)
+        assert flce.flce_check_device_error(ws) == 0
+        outs.append((loss, lse))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ref_loss, ref_lse = oracle.forward(X, W, y, wl.ignore_index, c["eps"], c["s"], c["red"])
+    ign = (y == wl.ignore_index).numpy()
+    lse = outs[1][1].cpu().double().numpy()
+    assert np.all(lse[ign] == 0.0)
+    if (~ign).any():
+        assert np.max(np.abs(lse[~ign] - ref_lse[~ign])) <= TOL_LSE_ABS
+    got = outs[1][0].cpu().double().numpy()
+    ref = np.atleast_1d(np.asarray(ref_loss, dtype=np.float64))
+    scale = np.maximum(np.abs(ref), 1.0) if c["red"] == "none" else np.maximum(np.abs(ref), 1e-30)
+    assert np.all(np.abs(got - ref) <= TOL_LOSS_REL * scale)

@@ -93,6 +93,11 @@ def test_noalloc_forward_matches_workspace_forward_and_oracle(gpu_lib):
                            zloss_scale=1e-4, reduction="mean"))
     _check_full(fn, custom("na2", 700, 256, 2048, seed=202, ignore_frac=0.05, reduction="sum"))
     _check_full(fn, custom("na3", 300, 64, 1024, seed=203, reduction="none"))
+    # room in the scratch for the forward on the valid rows (the workspace call above it
+    # runs on every row): the two must still agree bit for bit
+    big = custom("na6", 4096, 256, 8200, seed=206, ignore_frac=0.3, label_smoothing=0.05)
+    assert flce.flce_workspace_size(big.N, big.D, big.V, "forward_valid_rows") <= SCRATCH_BYTES
+    _check_full(fn, big)
     _check_full(fn, custom("na1", 1000, 136, 4104, seed=201, ignore_frac=0.1, label_smoothing=0.1,
                            zloss_scale=1e-4, reduction="mean"))
 

@@ -725,6 +725,7 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       WalkParams wg{};
       wg.total_tiles = int(n_tiles * vt);
       wg.tiles_minor = int(vt);
+      wg.minor_split = (FLCE_GRAD_MINOR_SPLIT > 1 && vt % FLCE_GRAD_MINOR_SPLIT == 0) ? FLCE_GRAD_MINOR_SPLIT : 1;
       wg.num_kb = int(cdiv(pb.D, kBK));
       wg.b_row_off = int(v0);
       wg.dyn_mode = DYN_ROW_GROUPS;

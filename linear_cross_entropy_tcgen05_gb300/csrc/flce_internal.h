@@ -61,6 +61,11 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_DW_MINOR_SPLIT
 #define FLCE_DW_MINOR_SPLIT 2
 #endif
+// Gradient GEMM: walk the band's vocabulary tiles in this many parts, each part across all
+// row groups before the next, so that the part's W slice stays in L2 with wide bands.
+#ifndef FLCE_GRAD_MINOR_SPLIT
+#define FLCE_GRAD_MINOR_SPLIT 1
+#endif
 // L2 policies (0 normal, 1 evict-first, 2 evict-last) of the dX GEMM's A operand (the
 // gradient band), the dW GEMM's operands, and the gradient GEMM's band store.
 #ifndef FLCE_DX_A_POL

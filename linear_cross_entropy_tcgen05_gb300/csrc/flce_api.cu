@@ -56,7 +56,7 @@ namespace {
 #define FLCE_L2_PROMOTION 3  // tensor-map L2 promotion: 0 none, 1 64 B, 2 128 B, 3 256 B
 #endif
 #ifndef FLCE_COMPACT_ROWS
-#define FLCE_COMPACT_ROWS 1  // 1: the backward GEMMs skip ignored rows (valid-row compaction)
+#define FLCE_COMPACT_ROWS 1  // 1: the GEMMs skip ignored rows (valid-row compaction; the forward with room for it)
 #endif
 
 constexpr size_t kHeaderBytes = 256;

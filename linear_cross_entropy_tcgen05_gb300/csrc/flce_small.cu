@@ -1,8 +1,9 @@
 // flce_small.cu -- the bandwidth/latency-bound helper kernels of fused linear
 // cross-entropy: the forward finalize (combine the vocabulary splits into lse, form the
 // row losses, reduce them in a fixed order), the backward prep (valid-row count and
-// per-row gradient coefficients), the valid-row compaction of the backward, and the
-// fp32 -> bf16 cast of dX.
+// per-row gradient coefficients), the valid-row compaction (row list and gather, for both
+// passes; the scatter back of dX), the fp32 -> bf16 cast of dX, and the launch counter and
+// GEMM timing diagnostics.
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -23,21 +24,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------------
 // ---------------------------------------------------------------------------------
 
-// Combine each row's partial statistics into lse and the row loss (FIN_LOSS), into one
-// vocabulary shard's statistics (FIN_SHARD_STATS), or combine K shards' statistics
-// (FIN_COMBINE); then reduce the loss deterministically (per-block fp64 partial sums,
-// then one block).
-// A forward GEMM whose pipeline wait ran out has set FLCE_DEVERR_TIMEOUT in this call's
-// error word (cleared when the call began) and left its partial statistics unwritten; they
-// may hold a previous call's values, so every result of this call is NaN instead.
-__device__ __forceinline__ bool forward_timed_out(const int* err) {
+// A GEMM whose pipeline wait ran out has set FLCE_DEVERR_TIMEOUT in this call's error word
+// (cleared when the call began) and left its outputs (the forward's partial statistics, a
+// part of the dX accumulator) unwritten; they may hold a previous call's values, so the
+// kernels that read them write NaN instead.
+__device__ __forceinline__ bool call_timed_out(const int* err) {
   return err != nullptr && (*reinterpret_cast<const volatile int*>(err) & FLCE_DEVERR_TIMEOUT) != 0;
 }
 
+// Combine each row's partial statistics into lse and the row loss (FIN_LOSS), into one
+// vocabulary shard's statistics (FIN_SHARD_STATS), or combine K shards' statistics
+// (FIN_COMBINE); then reduce the loss deterministically (per-block fp64 partial sums,
+// then one block). After a timeout every result of the call is NaN.
 __global__ void __launch_bounds__(kFinalizeThreads)
     flce_finalize_rows_kernel(const FinalizeParams p) {
   const int row = int(blockIdx.x) * kFinalizeThreads + int(threadIdx.x);
-  const bool timed_out = forward_timed_out(p.err);
+  const bool timed_out = call_timed_out(p.err);
   double contrib = 0.0, den = 0.0;
   int valid = 0, correct = 0;
   if (row < p.N) {
@@ -169,7 +171,7 @@ __global__ void __launch_bounds__(kFinalizeThreads)
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const bool timed_out = forward_timed_out(p.err);
+    const bool timed_out = call_timed_out(p.err);
     if (p.reduction != 2) {
       double total = ssum[0];
       if (p.reduction == 0) total = sden[0] != 0.0 ? total / sden[0] : 0.0;
@@ -305,11 +307,10 @@ __device__ __forceinline__ uint2 pack4_16bit(const float4 v) {
   }
 }
 
-// A backward GEMM whose pipeline wait ran out leaves parts of the dX accumulator
-// unwritten: the casts then write NaN to every dX element of the call.
+// After a timeout of a backward GEMM the casts write NaN to every dX element of the call.
 template <bool F16>
 __global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4, const int* err) {
-  const bool timed_out = forward_timed_out(err);
+  const bool timed_out = call_timed_out(err);
   const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
   for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x)
     dst[i] = pack4_16bit<F16>(timed_out ? nan4 : src[i]);
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(256) flce_scatter_cast_kernel(const ScatterCas
   const int lane = int(threadIdx.x) & 31;
   const int warps = int(gridDim.x) * (int(blockDim.x) >> 5);
   const int n4 = p.D / 4;
-  const bool timed_out = forward_timed_out(p.err);
+  const bool timed_out = call_timed_out(p.err);
   const float4 nan4 = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
   for (int r = int(blockIdx.x) * (int(blockDim.x) >> 5) + (int(threadIdx.x) >> 5); r < p.N; r += warps) {
     const int sl = p.slot[r];

@@ -689,6 +689,10 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
         "gpu_launches_per_step_expected": launches,
         "clocks": clk.summary(),
     }
+    # the step in SM cycles (time x median clock): comparable across boxes whose
+    # power-capped clocks differ
+    if out["clocks"].get("sm_mhz"):
+        out["mcycles_per_step"] = ms_step * out["clocks"]["sm_mhz"] / 1000.0
     if side is not None:
         out["workloads"] = side
     print(json.dumps(out), flush=True)

@@ -323,43 +323,65 @@ __global__ void flce_cast_kernel(const float4* __restrict__ src, uint2* __restri
 // accumulator's rows are cast back to their original places at the end.
 // ---------------------------------------------------------------------------------
 
-// One block: each thread takes a contiguous run of rows, the block scans the per-thread
-// counts of valid rows, and every thread writes its valid rows' indices in row order.
-__global__ void __launch_bounds__(1024) flce_compact_rows_kernel(const CompactParams p) {
-  __shared__ int warp_tot[32];
-  const int tid = int(threadIdx.x), lane = tid & 31, wid = tid >> 5;
-  const int per = (p.N + 1023) / 1024;
-  const int lo = min(p.N, tid * per), hi = min(p.N, lo + per);
-  int cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += p.targets[i] != p.ignore_index ? 1 : 0;
-  int inc = cnt;  // inclusive scan within the warp, then over the warps' totals
+// The list of valid rows in order, and each row's slot in it, by several blocks: block b
+// owns the rows [b R, (b + 1) R); it counts the valid rows before its range itself (a
+// coalesced pass over at most N targets, cheap next to the GEMMs), then walks its range in
+// tiles of 256 rows with a block-wide scan. No atomics and no waiting between blocks; the
+// last block writes the count.
+constexpr int kListThreads = 256;
+
+__device__ __forceinline__ int block_sum_int(int v, int* sh) {
+  const int lane = int(threadIdx.x) & 31, wid = int(threadIdx.x) >> 5;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  if (lane == 31) warp_tot[wid] = inc;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[wid] = v;
   __syncthreads();
-  if (wid == 0) {
-    int t = warp_tot[lane];
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kListThreads / 32; ++w) t += sh[w];
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(kListThreads) flce_compact_rows_kernel(const CompactParams p, int rows_per_block) {
+  __shared__ int sh[kListThreads / 32];
+  __shared__ int warp_tot[kListThreads / 32];
+  const int tid = int(threadIdx.x), lane = tid & 31, wid = tid >> 5;
+  const int lo = min(p.N, int(blockIdx.x) * rows_per_block);
+  const int hi = min(p.N, lo + rows_per_block);
+  int before = 0;
+  for (int i = tid; i < lo; i += kListThreads) before += p.targets[i] != p.ignore_index ? 1 : 0;
+  int pos = block_sum_int(before, sh);  // slot of this block's first valid row
+  for (int base = lo; base < hi; base += kListThreads) {
+    const int i = base + tid;
+    const int v = (i < hi && p.targets[i] != p.ignore_index) ? 1 : 0;
+    int inc = v;  // inclusive scan within the warp, then over the warps' totals
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += v;
+      const int x = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += x;
     }
-    warp_tot[lane] = t;
-  }
-  __syncthreads();
-  int pos = inc - cnt + (wid > 0 ? warp_tot[wid - 1] : 0);
-  for (int i = lo; i < hi; ++i) {
-    if (p.targets[i] != p.ignore_index) {
-      p.rows[pos] = i;
-      p.slot[i] = pos++;
-    } else {
-      p.slot[i] = -1;
+    if (lane == 31) warp_tot[wid] = inc;
+    __syncthreads();
+    int prior = 0, tile = 0;
+#pragma unroll
+    for (int w = 0; w < kListThreads / 32; ++w) {
+      prior += w < wid ? warp_tot[w] : 0;
+      tile += warp_tot[w];
     }
+    if (i < hi) {
+      if (v) {
+        const int at = pos + prior + inc - 1;
+        p.rows[at] = i;
+        p.slot[i] = at;
+      } else {
+        p.slot[i] = -1;
+      }
+    }
+    pos += tile;
+    __syncthreads();  // warp_tot is rewritten by the next tile
   }
-  if (tid == 1023) *p.n_valid = warp_tot[31];
+  if (blockIdx.x == gridDim.x - 1 && tid == 0) *p.n_valid = pos;
 }
 
 // Row i < n_valid of the compacted operands takes X row rows[i] and its coefficients;
@@ -541,7 +563,12 @@ cudaError_t launch_colsum(const ColsumParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_compact_rows(const CompactParams& p, cudaStream_t stream) {
-  flce_compact_rows_kernel<<<1, 1024, 0, stream>>>(p);
+  // ranges of at least 1024 rows, at most 256 blocks
+  int blocks = (p.N + 1023) / 1024;
+  if (blocks > 256) blocks = 256;
+  if (blocks < 1) blocks = 1;
+  const int per = (p.N + blocks - 1) / blocks;
+  flce_compact_rows_kernel<<<blocks, kListThreads, 0, stream>>>(p, per);
   count_launch();
   return cudaGetLastError();
 }

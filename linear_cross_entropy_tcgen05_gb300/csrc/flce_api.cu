@@ -725,7 +725,11 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       WalkParams wg{};
       wg.total_tiles = int(n_tiles * vt);
       wg.tiles_minor = int(vt);
-      wg.minor_split = (FLCE_GRAD_MINOR_SPLIT > 1 && vt % FLCE_GRAD_MINOR_SPLIT == 0) ? FLCE_GRAD_MINOR_SPLIT : 1;
+      if (FLCE_GRAD_SLICE_BYTES > 0) {
+        // parts of the band whose W slice (D x 256 columns x 2 bytes a tile) fits the budget
+        const int64_t parts = cdiv(pb.D * int64_t(kBN) * 2 * vt, FLCE_GRAD_SLICE_BYTES);
+        wg.minor_part = parts > 1 ? int(cdiv(vt, parts)) : 0;
+      }
       wg.num_kb = int(cdiv(pb.D, kBK));
       wg.b_row_off = int(v0);
       wg.dyn_mode = DYN_ROW_GROUPS;
@@ -773,7 +777,8 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
         ww.total_tiles = int(vt * d_tiles_m);
         ww.tiles_minor = int(d_tiles_m);
         ww.col_major = 1;
-        ww.minor_split = (FLCE_DW_MINOR_SPLIT > 1 && d_tiles_m % FLCE_DW_MINOR_SPLIT == 0) ? FLCE_DW_MINOR_SPLIT : 1;
+        ww.minor_part = (FLCE_DW_MINOR_SPLIT > 1 && d_tiles_m % FLCE_DW_MINOR_SPLIT == 0)
+                            ? int(d_tiles_m / FLCE_DW_MINOR_SPLIT) : 0;
         sw.x_off = int(v0);
         FLCE_CUDA_CHECK(launch_dw_gemm(tmXmn, tmGmn, tmDW, ww, sw, false, pb.f16, stream));
       } else {

@@ -321,13 +321,22 @@ struct WalkSched {
   __device__ bool next(Tile& t) {
     if (i >= w.total_tiles) return false;
     int major, minor;
-    if (w.minor_split > 1) {
-      const int m = w.tiles_minor / w.minor_split;  // minor tiles per part
-      const int per_part = (w.total_tiles / w.tiles_minor) * m;
-      const int part = i / per_part;
-      const int r = i - part * per_part;
-      major = r / m;
-      minor = part * m + (r - major * m);
+    if (w.minor_part > 0 && w.minor_part < w.tiles_minor) {
+      const int m = w.minor_part;                        // minor tiles per part
+      const int majors = w.total_tiles / w.tiles_minor;
+      const int full = w.tiles_minor / m;                // parts of m minors, then one of rest
+      const int per_part = majors * m;
+      if (i < full * per_part) {
+        const int part = i / per_part;
+        const int r = i - part * per_part;
+        major = r / m;
+        minor = part * m + (r - major * m);
+      } else {
+        const int rest = w.tiles_minor - full * m;
+        const int r = i - full * per_part;
+        major = r / rest;
+        minor = full * m + (r - major * rest);
+      }
     } else {
       major = i / w.tiles_minor;
       minor = i - major * w.tiles_minor;

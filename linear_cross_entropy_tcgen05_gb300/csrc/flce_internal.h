@@ -61,10 +61,11 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_DW_MINOR_SPLIT
 #define FLCE_DW_MINOR_SPLIT 2
 #endif
-// Gradient GEMM: walk the band's vocabulary tiles in this many parts, each part across all
-// row groups before the next, so that the part's W slice stays in L2 with wide bands.
-#ifndef FLCE_GRAD_MINOR_SPLIT
-#define FLCE_GRAD_MINOR_SPLIT 1
+// Gradient GEMM: walk the band's vocabulary tiles in parts whose W slice is at most this
+// many bytes, each part across all row groups before the next, so that the slice stays in
+// the L2 share that data read from both dies can use (0: one part).
+#ifndef FLCE_GRAD_SLICE_BYTES
+#define FLCE_GRAD_SLICE_BYTES (int64_t(40) << 20)
 #endif
 // L2 policies (0 normal, 1 evict-first, 2 evict-last) of the dX GEMM's A operand (the
 // gradient band), the dW GEMM's operands, and the gradient GEMM's band store.
@@ -107,8 +108,8 @@ struct WalkParams {
                      // column in flight), 0: over row-tile groups
   int dyn_mode;          // DynRows: how *dyn_rows bounds the walk (at least one group or block)
   const int* dyn_rows;   // device count of valid rows, or null
-  int minor_split;       // > 1: walk the minor tiles in this many parts, each part across all
-                         // majors before the next (tiles_minor divisible by it); 0 or 1: off
+  int minor_part;        // > 0: walk the minor tiles in parts of this many (the last part may
+                         // be narrower), each part across all majors before the next; 0: off
 };
 
 // Rows past the valid-row count that the compacted operands hold as zeros (with an

@@ -802,6 +802,11 @@ flce_status run_backward(const Problem& pb, const flce_options* opt, const float
       wx.b_k0 = int(v0);
       wx.dyn_mode = DYN_ROW_GROUPS;
       wx.dyn_rows = dyn;
+      if (FLCE_DX_SLICE_BYTES > 0) {
+        // parts of D's tiles whose slice of the band's W (256 rows x vc x 2 bytes a tile) fits
+        const int64_t parts = cdiv(int64_t(kBN) * vc * 2 * d_tiles_n, FLCE_DX_SLICE_BYTES);
+        wx.minor_part = parts > 1 ? int(cdiv(d_tiles_n, parts)) : 0;
+      }
       StoreEpiParams sx{band_i > 0 ? 1 : 0, 0, err, 0, out_scale, 1.f / kF16GradScale};
       FLCE_CUDA_CHECK(launch_dx_gemm(tmG, tmWx, tmDX, wx, sx, pb.w_vd, pb.f16, stream));
     }

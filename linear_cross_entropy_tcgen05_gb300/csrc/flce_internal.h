@@ -67,6 +67,11 @@ constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 #ifndef FLCE_GRAD_SLICE_BYTES
 #define FLCE_GRAD_SLICE_BYTES (int64_t(40) << 20)
 #endif
+// dX GEMM: the same for its D tiles (each reads a 256-row slice of the band's W); off by
+// default (measured even: the G rows are then read once per part).
+#ifndef FLCE_DX_SLICE_BYTES
+#define FLCE_DX_SLICE_BYTES int64_t(0)
+#endif
 // L2 policies (0 normal, 1 evict-first, 2 evict-last) of the dX GEMM's A operand (the
 // gradient band), the dW GEMM's operands, and the gradient GEMM's band store.
 #ifndef FLCE_DX_A_POL

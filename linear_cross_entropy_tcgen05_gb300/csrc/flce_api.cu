@@ -352,12 +352,15 @@ flce_status check_common(const void* X, const void* W, const int32_t* targets, i
 
 // The forward's units: cluster row blocks x vocabulary chunks (at most kMaxSplits chunks,
 // so at most that many partial statistics per row), walked panel by panel.
-void pick_forward_schedule(int64_t n_tiles, int64_t v_tiles, FwdParams* p) {
+void pick_forward_schedule(int64_t n_tiles, int64_t v_tiles, int64_t D, FwdParams* p) {
+  const int64_t block_rows = int64_t(gemm_pairs_per_cluster()) * kFwdRowBlock * gemm_tile_rows();
   const int64_t n_blocks = cdiv(n_tiles, int64_t(gemm_pairs_per_cluster()) * kFwdRowBlock);
   const int64_t chunk_tiles = cdiv(v_tiles, kMaxSplits);
   const int64_t n_chunks = cdiv(v_tiles, chunk_tiles);
+  int64_t panel = FLCE_FWD_PANEL > 0 ? int64_t(FLCE_FWD_PANEL) : FLCE_FWD_PANEL_BYTES / (block_rows * D * 2);
+  if (panel < 1) panel = 1;
   p->n_blocks = int(n_blocks);
-  p->panel = int(n_blocks < FLCE_FWD_PANEL ? n_blocks : FLCE_FWD_PANEL);
+  p->panel = int(n_blocks < panel ? n_blocks : panel);
   p->chunk_tiles = int(chunk_tiles);
   p->n_chunks = int(n_chunks);
   p->total_units = int(n_blocks * n_chunks);
@@ -530,7 +533,7 @@ flce_status run_forward(const Problem& pb, const flce_options* opt, int mode, in
   p.V = int(pb.V);
   p.n_tiles = int(n_tiles);
   p.v_tiles = int(v_tiles);
-  pick_forward_schedule(n_tiles, v_tiles, &p);
+  pick_forward_schedule(n_tiles, v_tiles, pb.D, &p);
   p.ticket = reinterpret_cast<int*>(ws + kHdrTicket);  // zeroed with the header above
   p.dyn_rows = compact ? n_valid : nullptr;
   p.row_of = compact ? rows : nullptr;

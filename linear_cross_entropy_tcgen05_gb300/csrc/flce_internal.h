@@ -40,9 +40,13 @@ constexpr int kMaxSplits = FLCE_FWD_MAX_SPLITS;
 constexpr int kFwdRowBlock = FLCE_FWD_ROW_BLOCK;
 // Forward: cluster row blocks per panel. The clusters working at one time take the
 // blocks of one panel through neighbouring vocabulary chunks, so they share the panel's
-// rows of X and the chunks' W tiles through L2.
+// rows of X and the chunks' W tiles through L2. FLCE_FWD_PANEL > 0 fixes the count;
+// 0 sizes the panel to FLCE_FWD_PANEL_BYTES of X (8 blocks at D = 4096).
 #ifndef FLCE_FWD_PANEL
-#define FLCE_FWD_PANEL 8
+#define FLCE_FWD_PANEL 0
+#endif
+#ifndef FLCE_FWD_PANEL_BYTES
+#define FLCE_FWD_PANEL_BYTES (int64_t(32) << 20)
 #endif
 // Diagnostic build: the GEMMs add the cycles their MMA thread waited for operands and
 // for the epilogue, its total cycles, and the cycles their producer waited for free

@@ -291,30 +291,48 @@ class Problem:
         if st != 0:
             raise RuntimeError(f"device error {where}: {self.flce.flce_status_string(st)}")
 
-    def timed_steps(self, steps, gpu_index):
+    def timed_steps(self, steps, gpu_index, kernel_timing=False):
         """`steps` forward + backward steps on the stream, each bracketed by CUDA events;
-        returns (total ms, per-step forward ms, per-step backward ms, launches, clocks)."""
+        returns (total ms, per-step forward ms, per-step backward ms, launches, clocks,
+        per-GEMM-kind timing). With kernel_timing the library also brackets every GEMM
+        launch of these steps with CUDA events on the stream (flce_profile_gemms), so each
+        GEMM kind's device time is measured over this same region."""
         flce = self.flce
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         torch.cuda.synchronize(self.dev)
+        if kernel_timing:
+            flce.flce_profile_read()  # nothing pending
         launches_before = flce.flce_kernel_launches()
         with ClockSampler(gpu_index) as clk:
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
-            start.record(self.stream)
-            for i in range(steps):
-                ev[i][0].record(self.stream)
-                self.fwd()
-                ev[i][1].record(self.stream)
-                self.bwd()
-                ev[i][2].record(self.stream)
-            end.record(self.stream)
+            if kernel_timing:
+                flce.flce_profile_gemms(True)
+            try:
+                start.record(self.stream)
+                for i in range(steps):
+                    ev[i][0].record(self.stream)
+                    self.fwd()
+                    ev[i][1].record(self.stream)
+                    self.bwd()
+                    ev[i][2].record(self.stream)
+                end.record(self.stream)
+            finally:
+                if kernel_timing:
+                    flce.flce_profile_gemms(False)
             launches = flce.flce_kernel_launches() - launches_before
             torch.cuda.synchronize(self.dev)
         self.check("in the timed region")
+        kinds = None
+        if kernel_timing:
+            kinds = {}
+            for kind, (ms, n) in flce.flce_profile_read().items():
+                if n:
+                    kinds[kind] = {"ms_per_step": ms / steps, "launches_per_step": n / steps, "avg_launch_ms": ms / n}
+            kinds = {"kinds": kinds, "steps": steps}
         return (start.elapsed_time(end), [a.elapsed_time(b) for a, b, _ in ev],
-                [b.elapsed_time(c) for _, b, c in ev], launches, clk)
+                [b.elapsed_time(c) for _, b, c in ev], launches, clk, kinds)
 
 
 def run_ours(args, wl):
@@ -373,16 +391,16 @@ def run_ours(args, wl):
     peak_alloc = torch.cuda.max_memory_allocated(dev)
     extra_bytes = peak_alloc - base_alloc
 
-    total_ms, fwd_ms, bwd_ms, launches_timed, clk = pb.timed_steps(args.steps, 0)
+    timing = not args.no_kernel_timing
+    total_ms, fwd_ms, bwd_ms, launches_timed, clk, kernels = pb.timed_steps(args.steps, 0, timing)
     # a run that saw thermal or hardware slowdown, or clocks held far below maximum with no
     # reason given (a leftover clock lock), is measured once more
     if clk.throttled():
-        total_ms, fwd_ms, bwd_ms, launches_timed, clk = pb.timed_steps(args.steps, 0)
+        total_ms, fwd_ms, bwd_ms, launches_timed, clk, kernels = pb.timed_steps(args.steps, 0, timing)
         clk.remeasured = True
     ms_step = total_ms / args.steps
     value = N / (ms_step / 1000.0)
     band_width = flce.flce_backward_band_width(N, D, V, pb.opt_b) or None
-    kernels = profile_gemm_kinds(pb, args.profile_steps)
 
     # end to end through the public API: pinned host inputs -> device, fwd+bwd, loss/dX/dW -> host
     e2e_value, e2e_ms, h2d, d2h = run_e2e(args, dev, stream, X, W, y, pb)
@@ -395,36 +413,6 @@ def run_ours(args, wl):
                   flce.flce_workspace_size(N, D, V, False),
                   flce.flce_workspace_size(args.row_band if 0 < args.row_band < N else N, D, V, True),
                   flce.flce_workspace_size(N, D, V, "forward_valid_rows"))
-
-
-def profile_gemm_kinds(pb, steps):
-    """Device time of each GEMM kind per step, measured live: `steps` more forward +
-    backward steps after the timed region with the library's launch events on
-    (flce_profile_gemms: a CUDA event pair on the call's stream around every GEMM
-    launch). Returns {kind: {"ms_per_step", "launches_per_step", "avg_launch_ms"}} and
-    the profiled steps' own time per step."""
-    flce = pb.flce
-    if steps <= 0:
-        return None
-    torch.cuda.synchronize(pb.dev)
-    flce.flce_profile_read()  # nothing pending
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flce.flce_profile_gemms(True)
-    try:
-        start.record(pb.stream)
-        for _ in range(steps):
-            pb.fwd()
-            pb.bwd()
-        end.record(pb.stream)
-        torch.cuda.synchronize(pb.dev)
-    finally:
-        flce.flce_profile_gemms(False)
-    pb.check("in the profiled steps")
-    out = {}
-    for kind, (ms, n) in flce.flce_profile_read().items():
-        if n:
-            out[kind] = {"ms_per_step": ms / steps, "launches_per_step": n / steps, "avg_launch_ms": ms / n}
-    return {"kinds": out, "step_ms": start.elapsed_time(end) / steps, "steps": steps}
 
 
 KERNEL_NAMES = {"forward": "flce_forward_gemm_kernel (forward GEMM + online softmax)",
@@ -564,9 +552,9 @@ def run_side_workloads(args, flce, dev, stream):
         pb.check(f"after the warm-up of {name}")
         peak = torch.cuda.max_memory_allocated(dev)
         # a short probe sets the step count for about side_seconds of timed work
-        t_probe, _, _, _, _ = pb.timed_steps(2, 0)
+        t_probe = pb.timed_steps(2, 0)[0]
         steps = int(min(400, max(5, math.ceil(args.side_seconds * 1000.0 / max(t_probe / 2, 1e-3)))))
-        total, f_ms, b_ms, launches, clk = pb.timed_steps(steps, 0)
+        total, f_ms, b_ms, launches, clk, _ = pb.timed_steps(steps, 0)
         step_ms = [f + b for f, b in zip(f_ms, b_ms)]
         med = statistics.median(step_ms)
         N, D, V = wl.N, wl.D, wl.V
@@ -642,8 +630,7 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
                     "share_of_gemm_time": dk["ms_per_step"] / sum(v["ms_per_step"] for v in per_kind.values()),
                     "frac_valid_rows": dk["achieved_valid_rows"] / sustained,
                     "measured": (f"CUDA events around every launch of the kind on its stream "
-                                 f"(flce_profile_gemms), {kernels['steps']} steps after the timed region "
-                                 f"({kernels['step_ms']:.2f} ms per profiled step)")}
+                                 f"(flce_profile_gemms), over the {kernels['steps']} steps of the timed region")}
     else:
         roofline = {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
                     "peak": sustained, "unit": "TFLOP/s", "frac": fwd_gemm_tf / sustained, "traffic": None,
@@ -734,8 +721,9 @@ def main():
     ap.add_argument("--side-workloads", default=SIDE_DEFAULT,
                     help="comma-separated workloads timed after the main one ('' for none)")
     ap.add_argument("--side-seconds", type=float, default=0.5, help="timed seconds per side workload")
-    ap.add_argument("--profile-steps", type=int, default=3,
-                    help="steps after the timed region with per-GEMM-kind device timing (0: none)")
+    ap.add_argument("--no-kernel-timing", action="store_true",
+                    help="time the region without the per-GEMM-kind events (the roofline then falls back to "
+                         "the forward call)")
     ap.add_argument("--wait-stats", action="store_true",
                     help="with --only and a library built with -DFLCE_WAIT_STATS=1: print pipeline wait shares")
     ap.add_argument("--only", choices=["fwd", "bwd"], default=None,

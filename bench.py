@@ -525,6 +525,36 @@ def device_inputs(wl, dev):
     return X, W, y
 
 
+GRAPH_BELOW_MS = 5.0  # side workloads whose step is this short are also timed as a replayed CUDA graph
+
+
+def graph_replay(pb, steps):
+    """One forward + backward step captured into a CUDA graph (the calls issue only stream
+    work, so they capture as they are) and replayed `steps` times back to back: the step
+    without the host's per-call cost, which is most of a small problem's time."""
+    graph = torch.cuda.CUDAGraph()
+    launch_stream = pb.stream
+    try:
+        with torch.cuda.graph(graph):
+            pb.stream = torch.cuda.current_stream(pb.dev)  # the capture stream
+            pb.fwd()
+            pb.bwd()
+    finally:
+        pb.stream = launch_stream
+    with torch.cuda.stream(launch_stream):
+        for _ in range(3):
+            graph.replay()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(launch_stream)
+        for _ in range(steps):
+            graph.replay()
+        end.record(launch_stream)
+    torch.cuda.synchronize(pb.dev)
+    pb.check("in the graph replays")
+    ms = start.elapsed_time(end) / steps
+    return {"ms_per_step": ms, "tokens_per_s": pb.wl.N / (ms / 1000.0), "replays": steps}
+
+
 def run_side_workloads(args, flce, dev, stream):
     """The other workloads and the memory-benchmark shape, each warmed up and then timed
     for about `args.side_seconds` (at least 5 steps): median fwd+bwd step, tokens/s, the
@@ -571,6 +601,8 @@ def run_side_workloads(args, flce, dev, stream):
             "launches_per_step": launches / steps,
             "clocks": clk.summary(),
         }
+        if med < GRAPH_BELOW_MS:
+            out[name]["graph"] = graph_replay(pb, steps)
         if name == "llama8k":
             out[name]["context"] = ("Liger-Kernel PR #1291, Benchmarks: CuTe-DSL FLCE fwd+bwd 25.7 ms at BT=8192, "
                                     "V=128256, H=4096, bf16, on B200 (another system and GPU)")

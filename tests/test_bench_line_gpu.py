@@ -48,3 +48,6 @@ def test_bench_line_carries_the_contract(gpu_lib):
     assert side["tokens_per_s"] > 0 and abs(side["tokens_per_s"] * side["ms_per_step_median"] / 1000 - 4096) < 1e-3
     # no N x V buffer: at this small N the gradient band spans half the vocabulary
     assert 0 < side["peak_mb"]["extra"] < side["peak_mb"]["logits_bf16_would_be"]
+    # a step this short is also timed as a replayed CUDA graph of the same calls
+    g = side["graph"]
+    assert g["replays"] == side["steps"] and 0 < g["ms_per_step"] < 10 * side["ms_per_step_median"]

@@ -151,6 +151,27 @@ def refuse_multi_gpu(args, world: int, rank: int) -> int:
     return 2
 
 
+L2_BYTES = 129e6  # GB300's L2
+
+
+def data_recipe(wl) -> str:
+    """The synthetic input recipe of a workload, for the JSON line's `data`."""
+    ign = f"{wl.ignore_frac:.0%} ignore_index" if wl.ignore_frac else "no ignored rows"
+    return f"synthetic (seeded; X~N(0,1), W~N(0,1/D) in bf16, {wl.target_dist} targets, {ign})"
+
+
+def l2_note(wl) -> str:
+    """Whether the inputs outsize the L2 (then no flush is needed between steps)."""
+    x, w = wl.N * wl.D * 2, wl.D * wl.V * 2
+    if min(x, w) > L2_BYTES:
+        return f"inputs larger than L2 (X {x / 1e9:.2f} GB, W {w / 1e9:.2f} GB > 129 MB); no flush"
+    if x + w > L2_BYTES:
+        return (f"inputs larger than L2 together (X {x / 1e6:.1f} MB + W {w / 1e6:.1f} MB > 129 MB); "
+                f"no flush")
+    return (f"inputs fit in the 129 MB L2 (X {x / 1e6:.2f} MB + W {w / 1e6:.2f} MB) and stay there between "
+            f"steps; no flush (a latency-bound size)")
+
+
 def kernel_launches_per_step(N, D, V, reduction, vc=None, compact=True, row_band=0, compact_fwd=True):
     """Kernels the library launches per step: (the forward's valid-row list and gather, with
     a workspace that has room for them) forward GEMM + finalize (+ loss reduction),
@@ -237,7 +258,7 @@ def run_reference(args, wl):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D), uniform targets, 5% ignored)",
+        "data": data_recipe(wl),
         "config": {"workload": wl.name, "N": wl.N, "D": wl.D, "V": wl.V, "reduction": wl.reduction,
                    "ignore_frac": wl.ignore_frac, "rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
@@ -672,10 +693,11 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; X~N(0,1), W~N(0,1/D) in bf16, uniform targets, 5% ignore_index)",
+        "data": data_recipe(wl),
         "config": {"workload": wl.name, "N": N, "D": D, "V": V, "reduction": wl.reduction,
-                   "ignore_frac": wl.ignore_frac, "grad_out": 1.0,
-                   "l2": "inputs larger than L2 (X 0.54 GB, W 1.05 GB > 129 MB); no flush",
+                   "ignore_frac": wl.ignore_frac, "label_smoothing": wl.label_smoothing,
+                   "zloss_scale": wl.zloss_scale, "grad_out": 1.0,
+                   "l2": l2_note(wl),
                    "parallelism": "one GPU", "vocab_band": vc, "bands": bands,
                    **({"row_band": args.row_band} if 0 < args.row_band < N else {})},
         # another system on another GPU: context, not a baseline

@@ -702,7 +702,9 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
                    **({"row_band": args.row_band} if 0 < args.row_band < N else {})},
         # another system on another GPU: context, not a baseline
         "context": {"liger_cutedsl_flce_b200": {
-            "tokens_per_s": liger_b200, "ratio": value / liger_b200,
+            "tokens_per_s": liger_b200,
+            # a ratio only where the figure's shape is the one measured here
+            "ratio": value / liger_b200 if (N, D, V) == (65536, 4096, 128256) else None,
             "source": "Liger-Kernel PR #1291, Benchmarks: 194 ms fwd+bwd at BT=65536, V=128256, H=4096, bf16, B200"}},
         "pct_bf16_peak": 100.0 * step_tf / burst,
         "tflops": step_tf,

@@ -688,7 +688,6 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
         roofline = {"kernel": "flce_forward_gemm_kernel", "bound": "tensor", "achieved": fwd_gemm_tf,
                     "peak": sustained, "unit": "TFLOP/s", "frac": fwd_gemm_tf / sustained, "traffic": None,
                     "traffic_source": None}
-    liger_b200 = 65536 / 0.194
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -702,9 +701,9 @@ def finish(args, wl, N, D, V, X, W, y, ms_step, value, fwd_ms, bwd_ms, peak_allo
                    **({"row_band": args.row_band} if 0 < args.row_band < N else {})},
         # another system on another GPU: context, not a baseline
         "context": {"liger_cutedsl_flce_b200": {
-            "tokens_per_s": liger_b200,
+            "tokens_per_s": PAGES_TOKENS_PER_S,
             # a ratio only where the figure's shape is the one measured here
-            "ratio": value / liger_b200 if (N, D, V) == (65536, 4096, 128256) else None,
+            "ratio": value / PAGES_TOKENS_PER_S if (N, D, V) == (65536, 4096, 128256) else None,
             "source": "Liger-Kernel PR #1291, Benchmarks: 194 ms fwd+bwd at BT=65536, V=128256, H=4096, bf16, B200"}},
         "pct_bf16_peak": 100.0 * step_tf / burst,
         "tflops": step_tf,
